@@ -1,0 +1,436 @@
+"""Benchmark of the dense GEMM hot path on GB300.
+
+Default workload: INT8 GEMM m = k = n = 4096 (A row-major, B K-major, int8
+uniform in [-128, 127], seed 1), int32 output; metric TOPS = 2*m*n*k / t.
+A step is one gemm_i8_run through the C ABI: plan lookup, int8 -> f16
+operand staging, tcgen05 tensor-core GEMM.  Inputs are resident in HBM and
+rotated through enough distinct input sets that they are never L2 hits.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   (the CPU oracle, timed alone)
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "INT8 GEMM TOPS (2mnk/s) and % of GB300 dense INT8 peak / HBM roofline"
+
+# name -> (workload, shape)
+BENCH_WORKLOADS = {
+    "i8_4096": ("i8_4096", (4096, 4096, 4096)),
+    "i8_256": ("i8_256", (256, 256, 256)),
+    "i8_8192": ("i8_ragged", (8192, 8192, 8192)),
+    "i8_4097x16384x255": ("i8_ragged", (4097, 16384, 255)),
+    "i8_1000x777x3000": ("i8_ragged", (1000, 777, 3000)),
+    "bf16_8192": ("bf16_8192", (8192, 8192, 8192)),
+    **{"i8_skinny_m%d" % m: ("i8_skinny", (m, 8192, 8192)) for m in (1, 8, 16, 32, 64, 128)},
+}
+
+DESCRIPTIONS = {
+    "i8_4096": "INT8 GEMM m=k=n=4096, A row-major, B K-major, int8 uniform [-128,127] seed 1, int32 out",
+    "i8_256": "INT8 GEMM m=k=n=256, int8 uniform [-128,127] seed 0, int32 out",
+    "i8_8192": "INT8 GEMM m=k=n=8192, int8 uniform [-128,127] seed 3, int32 out",
+    "i8_4097x16384x255": "INT8 GEMM (4097,16384,255), int8 uniform [-128,127] seed 3, int32 out",
+    "i8_1000x777x3000": "INT8 GEMM (1000,777,3000), int8 uniform [-128,127] seed 3, int32 out",
+    "bf16_8192": "BF16 GEMM m=k=n=8192, N(0,1) rounded to bf16 seed 4, fp32 accumulate and out",
+}
+for _m in (1, 8, 16, 32, 64, 128):
+    DESCRIPTIONS["i8_skinny_m%d" % _m] = ("INT8 skinny GEMM m=%d, k=n=8192, A U[-64,63], B round(32 N(0,1)) "
+                                          "clipped, seed 2, int32 out" % _m)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="i8_4096")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of the dominant kernels from the committed ncu
+    summary, keyed by workload, valid only for the kernel sources they were
+    measured on."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        if len(parts) >= 3:
+            out[parts[0]] = (float(parts[1]), parts[2])
+    return out
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_int8_matrix_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            self.out = ""
+            return False
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (getattr(self, "out", "") or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in rows:
+            if r["hw"].lower().startswith("active"):
+                reasons.add("hw_slowdown")
+            if r["hw_thermal"].lower().startswith("active"):
+                reasons.add("hw_thermal_slowdown")
+            if r["sw_thermal"].lower().startswith("active"):
+                reasons.add("sw_thermal_slowdown")
+            if r["sw_power"].lower().startswith("active"):
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len([r for r in rows if r["power"] > 200.0])}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+class OracleRunner:
+    """The CPU oracle on a bounded sample of a workload: the first R rows of C
+    (all n columns, full k).  Only this benchmark leg touches the oracle."""
+
+    def __init__(self, workload: str, shape):
+        import numpy as np
+
+        import oracle
+        from dense_int8_matrix_gb300 import workloads
+
+        oracle.build()
+        self.m, self.k, self.n = shape
+        A, Bt = workloads.make_inputs(workload, shape)
+        self.threads = host_cores()
+        if workloads.WORKLOADS[workload]["dtype"] == "i8":
+            An, Bn = A.numpy(), Bt.numpy()
+            self._run = lambda r: oracle.gemm_i8(An[:r], Bn, nthreads=self.threads)
+        else:
+            import torch
+            bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+            An, Bn = bits(A), bits(Bt)
+            self._run = lambda r: oracle.gemm_bf16(An[:r], Bn, nthreads=self.threads, with_abs=False)
+
+    def run(self, rows: int) -> float:
+        t0 = time.perf_counter()
+        self._run(rows)
+        return time.perf_counter() - t0
+
+    def rows_for(self, seconds: float) -> int:
+        cal = min(self.m, self.threads)
+        per_row = max(self.run(cal), 1e-6) / cal
+        rows = int(max(1, min(self.m, seconds / per_row)))
+        if rows >= self.threads:
+            rows = rows // self.threads * self.threads
+        return rows
+
+    def ops(self, rows: int) -> float:
+        return 2.0 * rows * self.n * self.k
+
+    def sample_text(self, rows: int) -> str:
+        return "first %d of %d rows of C (all %d columns, k=%d)" % (rows, self.m, self.n, self.k)
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    workload, shape = BENCH_WORKLOADS[args.workload]
+    m, k, n = shape
+    runner = OracleRunner(workload, shape)
+    budget = 120.0  # seconds for the whole reference run
+    rows = runner.rows_for(max(0.02, budget / max(1, args.steps + args.warmup)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = runner.run(rows)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1000.0 * statistics.mean(times)
+    value = runner.ops(rows) / (ms / 1000.0) / 1e12
+    is_i8 = workload != "bf16_8192"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS" if is_i8 else "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8->i64 exact" if is_i8 else "f64", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.workload], "m": m, "k": k, "n": n,
+                   "oracle": "plain C triple loop, rows split over POSIX threads"},
+        "cpu_baseline": {"value": value, "unit": "TOPS" if is_i8 else "TFLOP/s", "cores": runner.threads,
+                         "kind": "oracle", "sample": runner.sample_text(rows) + " per step"},
+        "e2e": {"value": value, "unit": "TOPS" if is_i8 else "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------ GPU path ----
+
+def run_ours(args):
+    import torch
+
+    from dense_int8_matrix_gb300 import binding as B
+    from dense_int8_matrix_gb300 import build as lib_build
+    from dense_int8_matrix_gb300 import workloads
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.cuda.current_device()
+    lib_build.build()
+    B.load()
+
+    workload, shape = BENCH_WORKLOADS[args.workload]
+    m, k, n = shape
+    is_i8 = workloads.WORKLOADS[workload]["dtype"] == "i8"
+    plan = B.gemm_i8_plan(m, k, n) if is_i8 else B.gemm_bf16_plan(m, k, n)
+    run = B.gemm_i8_run if is_i8 else B.gemm_bf16_run
+    run_host = B.gemm_i8_run_host if is_i8 else B.gemm_bf16_run_host
+    out_dtype = torch.int32 if is_i8 else torch.float32
+    esize = 1 if is_i8 else 2
+
+    # distinct input sets, together larger than 2x L2, so no step hits in L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = (m * k + n * k) * esize
+    nsets = max(2, min(64, -(-(2 * l2) // set_bytes)))
+    base_A, base_B = workloads.make_inputs(workload, shape)
+    sets = []
+    for s in range(nsets):
+        if s == 0:
+            A, Bt = base_A, base_B
+        else:
+            # cheap distinct copies: a per-set rotation of the rows
+            A = torch.roll(base_A, shifts=s, dims=0)
+            Bt = torch.roll(base_B, shifts=3 * s, dims=0)
+        sets.append((A.cuda(), Bt.cuda()))
+    C = torch.empty((m, n), dtype=out_dtype, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        A, Bt = sets[i % nsets]
+        run(plan, A, Bt, C, stream)
+    torch.cuda.synchronize()
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    B.gemm_trace_begin(4 * args.steps + 8)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            A, Bt = sets[i % nsets]
+            run(plan, A, Bt, C, stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    kernel_ms, launches = B.gemm_trace_collect()
+    st, code = B.gemm_device_error()
+    if st != B.GEMM_OK:
+        raise RuntimeError("device error during bench: code %d" % code)
+    max_ms = elapsed_ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+        dist.barrier()
+
+    ops = 2.0 * m * n * k
+    ms_per_step = max_ms / args.steps
+    value = world * ops / (ms_per_step / 1000.0) / 1e12
+
+    # end to end through the host-buffer entry point: H2D of A and Bt,
+    # the GEMM, D2H of C, inside the timed region
+    hA = base_A.pin_memory()
+    hB = base_B.pin_memory()
+    hC = torch.empty((m, n), dtype=out_dtype).pin_memory()
+    run_host(plan, hA, hB, hC, stream)
+    e2e_times = []
+    for _ in range(args.e2e_steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        run_host(plan, hA, hB, hC, stream)
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = statistics.median(e2e_times)
+    e2e_value = ops / e2e_s / 1e12
+
+    # roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    if plan.path == B.GEMM_PATH_SKINNY:
+        kind = B.GEMM_KERNEL_SKINNY
+        per_launch_ms = kernel_ms[kind] / max(1, launches[kind])
+        alg_bytes = m * k + n * k + 4 * m * n
+        achieved = alg_bytes / (per_launch_ms / 1000.0) / 1e9
+        roof = {"kernel": "skinny_dp4a", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_source": "%s hbm_gbs (STREAM-style copy)" % peak_src,
+                "algorithmic_bytes_per_launch": alg_bytes}
+        traffic_key = args.workload
+    else:
+        kind = B.GEMM_KERNEL_TC
+        per_launch_ms = kernel_ms[kind] / max(1, launches[kind])
+        achieved = ops / (per_launch_ms / 1000.0) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"kernel": "gemm_tc (tcgen05 kind::f16)", "bound": "tensor", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": ("%s bf16_tflops (burst cuBLAS bf16 GEMM); the int8 path runs on f16 "
+                                "tensor-core MMAs, whose nominal dense rate equals bf16's" % peak_src),
+                "algorithmic_flops_per_launch": ops}
+        traffic_key = args.workload
+    traffic = load_traffic().get(traffic_key)
+    digest = kernel_source_digest()
+    roof["traffic"] = traffic[0] if traffic and traffic[1] == digest else None
+    roof["kernel_ms_per_launch"] = per_launch_ms
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS" if is_i8 else "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8->i32 exact (f16 tensor-core MMA, fp32 chunks <= 2^24, int32 sum)" if is_i8
+        else "bf16->f32 (fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.workload], "m": m, "k": k, "n": n,
+                   "l2": "inputs rotated over %d distinct sets (%d MiB) > 2x L2 (%d MiB)"
+                         % (nsets, nsets * set_bytes >> 20, l2 >> 20),
+                   "plan": {"path": "tensor" if plan.path == 0 else "skinny", "bm": plan.bm,
+                            "bn": plan.bn, "grid": plan.grid, "tiles": plan.tiles, "waves": plan.waves,
+                            "num_sms": plan.num_sms},
+                   "parallelism": "replicas" if world > 1 else "single-gpu"},
+        "gpu_launches": int(sum(launches)),
+        "gpu_launches_by_kind": {"stage": launches[0], "tc": launches[1], "skinny": launches[2]},
+        "kernel_ms_by_kind": {"stage": kernel_ms[0], "tc": kernel_ms[1], "skinny": kernel_ms[2]},
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": "TOPS" if is_i8 else "TFLOP/s",
+                "h2d_bytes_per_step": (m * k + n * k) * esize, "d2h_bytes_per_step": m * n * 4,
+                "ms_per_step": e2e_s * 1000.0},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        runner = OracleRunner(workload, shape)
+        rows = runner.rows_for(args.cpu_seconds)
+        dt = runner.run(rows)
+        line["cpu_baseline"] = {"value": runner.ops(rows) / dt / 1e12, "unit": line["unit"],
+                                "cores": runner.threads, "kind": "oracle",
+                                "sample": runner.sample_text(rows) + ": %.1f s" % dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

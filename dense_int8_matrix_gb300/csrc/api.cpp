@@ -1,0 +1,351 @@
+// C ABI of the library: argument checks, per-device state, workspace from a
+// private stream-ordered pool, dispatch to the kernels, tracing.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/dense_int8_matrix.h"
+#include "internal.h"
+
+namespace gemm {
+gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t num_sms, gemm_plan* out);
+}
+
+using namespace gemm;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    int* err_word = nullptr;
+    cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Per-device state, created on first use with that device current.
+gemm_status device_state(DeviceState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        s.num_sms = sms;
+        s.supported = (major == 10 && minor == 3);
+        if (s.supported) {
+            if (cudaMalloc(reinterpret_cast<void**>(&s.err_word), sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+            if (cudaMemset(s.err_word, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+            cudaMemPoolProps props;
+            std::memset(&props, 0, sizeof(props));
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            if (cudaMemPoolCreate(&s.pool, &props) != cudaSuccess) return GEMM_ERR_CUDA;
+            uint64_t keep = UINT64_MAX;  // keep freed scratch for the next call
+            if (cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        }
+        s.ready = true;
+    }
+    *out = &s;
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------- tracing --
+struct TraceRec {
+    int kind;
+    cudaEvent_t start, stop;
+};
+
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+size_t g_trace_used = 0;
+
+struct TraceScope {
+    TraceRec* rec = nullptr;
+    cudaStream_t stream;
+    TraceScope(int kind, cudaStream_t s) : stream(s) {
+        std::lock_guard<std::mutex> lock(g_trace_mu);
+        if (g_trace_on && g_trace_used < g_trace.size()) {
+            rec = &g_trace[g_trace_used++];
+            rec->kind = kind;
+            cudaEventRecord(rec->start, stream);
+        }
+    }
+    ~TraceScope() {
+        if (rec) cudaEventRecord(rec->stop, stream);
+    }
+};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+gemm_status check_plan(const gemm_plan* p, int32_t dtype) {
+    if (!p || p->version != GEMM_PLAN_VERSION || p->dtype != dtype) return GEMM_ERR_INVALID_ARG;
+    if (p->m < 1 || p->k < 1 || p->n < 1) return GEMM_ERR_INVALID_ARG;
+    if (p->path == GEMM_PATH_SKINNY) {
+        if (dtype != GEMM_DTYPE_I8 || p->m > 64 || p->grid < 1) return GEMM_ERR_INVALID_ARG;
+        return GEMM_OK;
+    }
+    if (p->path != GEMM_PATH_TENSOR) return GEMM_ERR_INVALID_ARG;
+    // a plan may be edited to force a tile, but only to one that is compiled
+    if (p->bm != 64 && p->bm != 128) return GEMM_ERR_INVALID_ARG;
+    if (p->bn != 32 && p->bn != 64 && p->bn != 128 && p->bn != 256) return GEMM_ERR_INVALID_ARG;
+    if (p->grid < 1 || p->k_pitch < p->k || (p->k_pitch % 8) != 0 || p->chunk_k < kTcBK ||
+        (p->chunk_k % kTcBK) != 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (dtype == GEMM_DTYPE_I8 && p->chunk_k > kI8ChunkK) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* C, cudaStream_t stream) {
+    DeviceState* ds = nullptr;
+    gemm_status st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    if (!ds->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!tensor_map_encoder_available() && p->path == GEMM_PATH_TENSOR) return GEMM_ERR_CUDA;
+
+    if (p->path == GEMM_PATH_SKINNY) {
+        TraceScope t(GEMM_KERNEL_SKINNY, stream);
+        if (launch_skinny_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), static_cast<int32_t*>(C),
+                             p->m, p->n, p->k, ds->num_sms, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return GEMM_OK;
+    }
+
+    const bool is_i8 = p->dtype == GEMM_DTYPE_I8;
+    const bool need_stage = is_i8 || (p->k_pitch != p->k);
+    void* ws = nullptr;
+    const void* A16 = A;
+    const void* B16 = Bt;
+    if (need_stage) {
+        const int64_t a_bytes = ((p->m * p->k_pitch * 2 + 255) / 256) * 256;
+        const int64_t b_bytes = ((p->n * p->k_pitch * 2 + 255) / 256) * 256;
+        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes), ds->pool, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        uint16_t* Ah = static_cast<uint16_t*>(ws);
+        uint16_t* Bh = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + a_bytes);
+        cudaError_t e;
+        {
+            TraceScope t(GEMM_KERNEL_STAGE, stream);
+            if (is_i8)
+                e = launch_stage_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), Ah, Bh, p->m, p->n,
+                                    p->k, p->k_pitch, ds->num_sms, stream);
+            else
+                e = launch_stage_b16(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(Bt), Ah, Bh, p->m,
+                                     p->n, p->k, p->k_pitch, ds->num_sms, stream);
+        }
+        if (e != cudaSuccess) {
+            cudaFreeAsync(ws, stream);
+            return GEMM_ERR_CUDA;
+        }
+        A16 = Ah;
+        B16 = Bh;
+    }
+
+    TcLaunch L;
+    L.A16 = A16;
+    L.B16 = B16;
+    L.C = C;
+    L.err = ds->err_word;
+    L.m = p->m;
+    L.n = p->n;
+    L.k = p->k;
+    L.k_pitch = p->k_pitch;
+    L.bm = p->bm;
+    L.bn = p->bn;
+    L.grid = p->grid;
+    L.chunk_kb = p->chunk_k / kTcBK;
+    L.int_out = is_i8;
+    cudaError_t e;
+    {
+        TraceScope t(GEMM_KERNEL_TC, stream);
+        e = launch_tc(L, stream);
+    }
+    if (ws) cudaFreeAsync(ws, stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status check_ptrs(const void* A, const void* Bt, const void* C) {
+    if (!A || !Bt || !C) return GEMM_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(Bt, 16) || !aligned(C, 4)) return GEMM_ERR_MISALIGNED;
+    return GEMM_OK;
+}
+
+gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const void* Bt, void* C, cudaStream_t stream) {
+    gemm_status st = check_plan(p, dtype);
+    if (st != GEMM_OK) return st;
+    if (!A || !Bt || !C) return GEMM_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    if (!ds->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    const size_t es = dtype == GEMM_DTYPE_I8 ? 1 : 2;
+    const size_t a_bytes = static_cast<size_t>(p->m * p->k) * es;
+    const size_t b_bytes = static_cast<size_t>(p->n * p->k) * es;
+    const size_t c_bytes = static_cast<size_t>(p->m * p->n) * 4;
+    const size_t a_al = (a_bytes + 255) / 256 * 256, b_al = (b_bytes + 255) / 256 * 256;
+    void* buf = nullptr;
+    if (cudaMallocFromPoolAsync(&buf, a_al + b_al + c_bytes, ds->pool, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    char* dA = static_cast<char*>(buf);
+    char* dB = dA + a_al;
+    char* dC = dB + b_al;
+    st = GEMM_OK;
+    if (cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(dB, Bt, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        st = GEMM_ERR_CUDA;
+    if (st == GEMM_OK) st = run_device(p, dA, dB, dC, stream);
+    if (st == GEMM_OK && cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        st = GEMM_ERR_CUDA;
+    cudaFreeAsync(buf, stream);
+    if (cudaStreamSynchronize(stream) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status gemm_plan_for_sms(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t num_sms, gemm_plan* out) {
+    return make_plan(dtype, m, k, n, num_sms, out);
+}
+
+static gemm_status plan_current(int32_t dtype, int64_t m, int64_t k, int64_t n, gemm_plan* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    // argument errors first, without touching the device
+    gemm_plan probe;
+    gemm_status st = make_plan(dtype, m, k, n, 148, &probe);
+    if (st != GEMM_OK) return st;
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    return make_plan(dtype, m, k, n, ds->num_sms, out);
+}
+
+gemm_status gemm_i8_plan(int64_t m, int64_t k, int64_t n, gemm_plan* out) {
+    return plan_current(GEMM_DTYPE_I8, m, k, n, out);
+}
+
+gemm_status gemm_bf16_plan(int64_t m, int64_t k, int64_t n, gemm_plan* out) {
+    return plan_current(GEMM_DTYPE_BF16, m, k, n, out);
+}
+
+gemm_status gemm_i8_run(const gemm_plan* plan, const int8_t* A, const int8_t* Bt, int32_t* C, void* stream) {
+    gemm_status st = check_plan(plan, GEMM_DTYPE_I8);
+    if (st != GEMM_OK) return st;
+    st = check_ptrs(A, Bt, C);
+    if (st != GEMM_OK) return st;
+    return run_device(plan, A, Bt, C, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status gemm_bf16_run(const gemm_plan* plan, const uint16_t* A, const uint16_t* Bt, float* C, void* stream) {
+    gemm_status st = check_plan(plan, GEMM_DTYPE_BF16);
+    if (st != GEMM_OK) return st;
+    st = check_ptrs(A, Bt, C);
+    if (st != GEMM_OK) return st;
+    return run_device(plan, A, Bt, C, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status gemm_i8_run_host(const gemm_plan* plan, const int8_t* A, const int8_t* Bt, int32_t* C, void* stream) {
+    return run_host(plan, GEMM_DTYPE_I8, A, Bt, C, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status gemm_bf16_run_host(const gemm_plan* plan, const uint16_t* A, const uint16_t* Bt, float* C,
+                               void* stream) {
+    return run_host(plan, GEMM_DTYPE_BF16, A, Bt, C, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status gemm_device_error(void* stream, int32_t* code) {
+    if (code) *code = 0;
+    DeviceState* ds = nullptr;
+    gemm_status st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    if (!ds->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ds->err_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (v == 0) return GEMM_OK;
+    if (code) *code = v;
+    if (cudaMemset(ds->err_word, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+    return GEMM_ERR_TIMEOUT;
+}
+
+gemm_status gemm_trace_begin(int32_t capacity) {
+    if (capacity < 0) return GEMM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    while (g_trace.size() < static_cast<size_t>(capacity)) {
+        TraceRec r;
+        r.kind = 0;
+        if (cudaEventCreate(&r.start) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaEventCreate(&r.stop) != cudaSuccess) {
+            cudaEventDestroy(r.start);
+            return GEMM_ERR_CUDA;
+        }
+        g_trace.push_back(r);
+    }
+    g_trace_used = 0;
+    g_trace_on = true;
+    return GEMM_OK;
+}
+
+gemm_status gemm_trace_collect(float* ms_per_kind, int32_t* launches_per_kind) {
+    if (!ms_per_kind || !launches_per_kind) return GEMM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    for (int i = 0; i < GEMM_KERNEL_KINDS; ++i) {
+        ms_per_kind[i] = 0.f;
+        launches_per_kind[i] = 0;
+    }
+    gemm_status st = GEMM_OK;
+    for (size_t i = 0; i < g_trace_used; ++i) {
+        TraceRec& r = g_trace[i];
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) {
+            st = GEMM_ERR_CUDA;
+            continue;
+        }
+        if (r.kind >= 0 && r.kind < GEMM_KERNEL_KINDS) {
+            ms_per_kind[r.kind] += ms;
+            launches_per_kind[r.kind] += 1;
+        }
+    }
+    g_trace_on = false;
+    g_trace_used = 0;
+    return st;
+}
+
+gemm_status gemm_tc_kernel_info(int32_t bm, int32_t bn, int32_t dtype, int32_t* regs, int32_t* ctas_per_sm) {
+    if (!regs || !ctas_per_sm) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_DTYPE_I8 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    *regs = tc_num_regs(bm, bn, dtype == GEMM_DTYPE_I8);
+    *ctas_per_sm = tc_occupancy(bm, bn, dtype == GEMM_DTYPE_I8);
+    return *regs < 0 ? GEMM_ERR_INVALID_ARG : GEMM_OK;
+}
+
+const char* gemm_status_string(gemm_status s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+        case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED";
+        case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+        case GEMM_ERR_OVERFLOW_RISK: return "GEMM_ERR_OVERFLOW_RISK";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+}  // extern "C"

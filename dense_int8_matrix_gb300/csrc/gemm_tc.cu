@@ -1,0 +1,412 @@
+// Tensor-core GEMM for sm_103a: C = A x B with A (m x k) and B stored K-major
+// as Bt (n x k), both staged as 16-bit operands (f16 holding exact int8
+// values, or bf16), fp32 accumulation in TMEM, int32 or fp32 output.
+//
+// Structure (one persistent CTA per SM slot, 12 warps):
+//   warp 0      TMA producer: copies the A tile (BM x 64) and the Bt tile
+//               (BN x 64) of each K step into a 4-stage shared-memory ring
+//               (128-byte swizzle), signalling a "full" mbarrier per stage.
+//               This multi-stage ring is the double-buffered prefetch of
+//               "CUDA编程实践" §3 (数据prefetch) taken to four stages.
+//   warp 1      allocates TMEM and issues tcgen05.mma (M = BM, N = BN, K = 16,
+//               four per stage) into one of two TMEM accumulators; each
+//               stage is released to the producer by tcgen05.commit.
+//   warps 4-11  epilogue: tcgen05.ld the accumulator, fold it into running
+//               sums held in registers, release the accumulator, and after
+//               the last K chunk of a tile write C with vector stores.
+// The two accumulators alternate per K chunk, so the epilogue of one chunk
+// (or tile) overlaps the MMAs of the next.
+//
+// For int8 problems the accumulator is drained every 1024 K elements and
+// converted to int32 exactly (see kI8ChunkK), so the result is bit-exact for
+// every int8 input up to the library's k limit.  For bf16 problems a chunk is
+// the whole K loop.
+//
+// Tile order: tiles are visited in bands of 8 M-tiles, N fastest within a
+// band, so that the CTAs running together share A and B panels in L2 (the
+// swizzled block mapping of "先导杯比赛回顾", section "Swizzle 线程块映射").
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gemm {
+
+namespace {
+
+template <int BM, int BN>
+struct TcCfg {
+    static constexpr int A_BYTES = BM * kTcRowBytes;
+    static constexpr int B_BYTES = BN * kTcRowBytes;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = tc_tmem_cols(BN);
+    static constexpr int HALF = BN / 2;                 // columns per epilogue thread
+    static constexpr int SLICE = HALF >= 32 ? 32 : 16;  // columns per tcgen05.ld
+    static constexpr int NSLICE = HALF / SLICE;
+    static constexpr size_t SMEM = tc_smem_bytes(BM, BN);
+    static_assert(BM == 64 || BM == 128, "BM");
+    static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN");
+    static_assert(kTcStages * STAGE_BYTES + 1024 + 8 * (2 * kTcStages + 5) + 8 <= SMEM, "smem layout");
+};
+
+struct TcParams {
+    void* C;
+    int* err;
+    int64_t m, n;
+    int num_kb;     // ceil(k / 64)
+    int chunk_kb;   // K steps per accumulator chunk
+    int tiles_m, tiles_n, tiles;
+};
+
+constexpr int kBandM = 8;
+
+__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
+    const int per_band = kBandM * p.tiles_n;
+    const int band = t / per_band;
+    const int first_m = band * kBandM;
+    const int rows_in_band = min(kBandM, p.tiles_m - first_m);
+    const int local = t - band * per_band;
+    tm = first_m + local % rows_in_band;
+    tn = local / rows_in_band;
+}
+
+template <int BM, int BN, bool INT_OUT>
+__global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+    using Cfg = TcCfg<BM, BN>;
+    extern __shared__ uint8_t smem_raw[];
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t sA = base;
+    const uint32_t sB = base + kTcStages * Cfg::A_BYTES;
+    uint8_t* ctrl = smem_raw + (base - raw) + kTcStages * Cfg::STAGE_BYTES;
+    const uint32_t bar0 = smem_u32(ctrl);
+    // barrier slots: full[S], empty[S], acc_full[2], acc_empty[2], done
+    const uint32_t full_bar0 = bar0;
+    const uint32_t empty_bar0 = bar0 + 8u * kTcStages;
+    const uint32_t accf_bar0 = bar0 + 16u * kTcStages;
+    const uint32_t acce_bar0 = accf_bar0 + 16u;
+    const uint32_t done_bar = acce_bar0 + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kTcStages + 5));
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(full_bar0 + 8u * s, 1);
+            mbar_init(empty_bar0 + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar0 + 8u * b, 1);
+            mbar_init(acce_bar0 + 8u * b, kTcEpilogueWarps);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer --
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            const uint64_t pol = policy_evict_normal();
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(t, p, tm, tn);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    const uint32_t s = issued % kTcStages;
+                    const uint32_t ph = (issued / kTcStages) & 1u;
+                    if (!wait_bounded(empty_bar0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar0 + 8u * s, Cfg::STAGE_BYTES);
+                    tma_load_2d(sA + s * Cfg::A_BYTES, &tmA, kb * kTcBK, tm * BM, full_bar0 + 8u * s, pol);
+                    tma_load_2d(sB + s * Cfg::B_BYTES, &tmB, kb * kTcBK, tn * BN, full_bar0 + 8u * s, pol);
+                    ++issued;
+                }
+            }
+            // Teardown: every copy started must land before the CTA exits.
+            for (uint32_t s = 0; s < static_cast<uint32_t>(kTcStages) && s < issued; ++s) {
+                const uint32_t last = s + ((issued - 1u - s) / kTcStages) * kTcStages;
+                wait_bounded(full_bar0 + 8u * s, (last / kTcStages) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer --
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(INT_OUT ? 0u : 1u, BM, BN);
+            uint32_t consumed = 0, acc_iter = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+                for (int c0 = 0; ok && c0 < p.num_kb; c0 += p.chunk_kb) {
+                    const uint32_t buf = acc_iter & 1u;
+                    const uint32_t aph = (acc_iter >> 1) & 1u;
+                    if (!wait_bounded(acce_bar0 + 8u * buf, aph ^ 1u, abort_flag, p.err, kDevErrTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const int c1 = min(p.num_kb, c0 + p.chunk_kb);
+                    for (int kb = c0; kb < c1; ++kb) {
+                        const uint32_t s = consumed % kTcStages;
+                        const uint32_t ph = (consumed / kTcStages) & 1u;
+                        if (!wait_bounded(full_bar0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t adesc = smem_desc_sw128_kmajor(sA + s * Cfg::A_BYTES);
+                        const uint64_t bdesc = smem_desc_sw128_kmajor(sB + s * Cfg::B_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                            // K step of 16 elements = 32 bytes = 2 in the >>4 address field
+                            mma_f16_ss(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                       (kb > c0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(empty_bar0 + 8u * s);
+                        ++consumed;
+                    }
+                    if (!ok) break;
+                    mma_commit(accf_bar0 + 8u * buf);
+                    ++acc_iter;
+                }
+            }
+            // Teardown: all MMAs issued must complete before TMEM is freed.
+            mma_commit(done_bar);
+            wait_bounded(done_bar, 0u, nullptr, p.err, kDevErrTimeoutTeardown);
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------------------- epilogue --
+        const int e = warp - 4;
+        const int q = warp & 3;     // TMEM lane quarter this warp can access
+        const int h = e >> 2;       // which half of the BN columns
+        using Acc = typename std::conditional<INT_OUT, int32_t, float>::type;
+        uint32_t acc_iter = 0;
+        bool ok = true;
+        const bool row_valid = (BM == 128) || (lane < 16);
+        const int row_in_tile = (BM == 128) ? (q * 32 + lane) : (q * 16 + lane);
+        for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, p, tm, tn);
+            Acc acc[Cfg::HALF];
+#pragma unroll
+            for (int j = 0; j < Cfg::HALF; ++j) acc[j] = Acc(0);
+            for (int c0 = 0; c0 < p.num_kb; c0 += p.chunk_kb) {
+                const uint32_t buf = acc_iter & 1u;
+                const uint32_t aph = (acc_iter >> 1) & 1u;
+                // lane 0 polls; the warp then reconverges before the
+                // warp-collective tcgen05.ld
+                int got = 1;
+                if (lane == 0)
+                    got = wait_bounded(accf_bar0 + 8u * buf, aph, abort_flag, p.err, kDevErrTimeoutEpilogue) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * Cfg::HALF;
+#pragma unroll
+                for (int sl = 0; sl < Cfg::NSLICE; ++sl) {
+                    uint32_t r[Cfg::SLICE];
+                    if constexpr (Cfg::SLICE == 32)
+                        tmem_ld_32x32b_x32(tcol + sl * 32, r);
+                    else
+                        tmem_ld_32x32b_x16(tcol + sl * 16, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < Cfg::SLICE; ++j) {
+                        const float v = __uint_as_float(r[j]);
+                        if constexpr (INT_OUT)
+                            acc[sl * Cfg::SLICE + j] += __float2int_rn(v);   // exact: |v| <= 2^24
+                        else
+                            acc[sl * Cfg::SLICE + j] += v;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce_bar0 + 8u * buf);
+                ++acc_iter;
+            }
+            if (!ok) break;
+            const int64_t row = static_cast<int64_t>(tm) * BM + row_in_tile;
+            const int64_t col0 = static_cast<int64_t>(tn) * BN + h * Cfg::HALF;
+            if (row_valid && row < p.m) {
+                Acc* out = static_cast<Acc*>(p.C) + row * p.n + col0;
+                const bool vec = ((p.n & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
+                                 (col0 + Cfg::HALF <= p.n);
+                if (vec) {
+#pragma unroll
+                    for (int j = 0; j < Cfg::HALF; j += 4) {
+                        int4 v;
+                        if constexpr (INT_OUT) {
+                            v = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                        } else {
+                            v = make_int4(__float_as_int(acc[j]), __float_as_int(acc[j + 1]),
+                                          __float_as_int(acc[j + 2]), __float_as_int(acc[j + 3]));
+                        }
+                        *reinterpret_cast<int4*>(out + j) = v;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < Cfg::HALF; ++j)
+                        if (col0 + j < p.n) out[j] = acc[j];
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host ----
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor map of a rows x k 16-bit operand with row pitch k_pitch elements,
+// box = 64 elements (128 bytes) x box_rows, 128-byte swizzle; elements outside
+// [0,k) x [0,rows) read as zero.
+bool encode_operand_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t k, int64_t k_pitch,
+                        int box_rows) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k_pitch) * 2u};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BM, int BN, bool INT_OUT>
+cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
+    using Cfg = TcCfg<BM, BN>;
+    auto kern = gemm_tc_kernel<BM, BN, INT_OUT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::SMEM));
+    if (e != cudaSuccess) return e;
+    CUtensorMap mA, mB;
+    if (!encode_operand_map(&mA, a.A16, a.m, a.k, a.k_pitch, BM)) return cudaErrorInvalidValue;
+    if (!encode_operand_map(&mB, a.B16, a.n, a.k, a.k_pitch, BN)) return cudaErrorInvalidValue;
+    TcParams p;
+    p.C = a.C;
+    p.err = a.err;
+    p.m = a.m;
+    p.n = a.n;
+    p.num_kb = static_cast<int>((a.k + kTcBK - 1) / kTcBK);
+    p.chunk_kb = a.chunk_kb;
+    p.tiles_m = static_cast<int>((a.m + BM - 1) / BM);
+    p.tiles_n = static_cast<int>((a.n + BN - 1) / BN);
+    p.tiles = p.tiles_m * p.tiles_n;
+    kern<<<a.grid, kTcThreads, Cfg::SMEM, stream>>>(mA, mB, p);
+    return cudaGetLastError();
+}
+
+template <bool INT_OUT>
+cudaError_t dispatch(const TcLaunch& a, cudaStream_t stream) {
+#define GEMM_TC_CASE(BM_, BN_) \
+    if (a.bm == BM_ && a.bn == BN_) return launch_one<BM_, BN_, INT_OUT>(a, stream);
+    GEMM_TC_CASE(128, 256)
+    GEMM_TC_CASE(128, 128)
+    GEMM_TC_CASE(128, 64)
+    GEMM_TC_CASE(128, 32)
+    GEMM_TC_CASE(64, 256)
+    GEMM_TC_CASE(64, 128)
+    GEMM_TC_CASE(64, 64)
+    GEMM_TC_CASE(64, 32)
+#undef GEMM_TC_CASE
+    return cudaErrorInvalidValue;
+}
+
+template <int BM, int BN, bool INT_OUT>
+const void* kernel_ptr() {
+    return reinterpret_cast<const void*>(gemm_tc_kernel<BM, BN, INT_OUT>);
+}
+
+const void* find_kernel(int bm, int bn, bool int_out) {
+#define GEMM_TC_PTR(bm_, bn_)                                                                   \
+    if (bm == bm_ && bn == bn_)                                                                 \
+        return int_out ? kernel_ptr<bm_, bn_, true>() : kernel_ptr<bm_, bn_, false>();
+    GEMM_TC_PTR(128, 256)
+    GEMM_TC_PTR(128, 128)
+    GEMM_TC_PTR(128, 64)
+    GEMM_TC_PTR(128, 32)
+    GEMM_TC_PTR(64, 256)
+    GEMM_TC_PTR(64, 128)
+    GEMM_TC_PTR(64, 64)
+    GEMM_TC_PTR(64, 32)
+#undef GEMM_TC_PTR
+    return nullptr;
+}
+
+}  // namespace
+
+bool tensor_map_encoder_available() { return get_encoder() != nullptr; }
+
+cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream) {
+    return a.int_out ? dispatch<true>(a, stream) : dispatch<false>(a, stream);
+}
+
+int tc_occupancy(int bm, int bn, bool int_out) {
+    const void* k = find_kernel(bm, bn, int_out);
+    if (!k) return 0;
+    const size_t smem = tc_smem_bytes(bm, bn);
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+        return 0;
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, kTcThreads, smem) != cudaSuccess) return 0;
+    return blocks;
+}
+
+int tc_num_regs(int bm, int bn, bool int_out) {
+    const void* k = find_kernel(bm, bn, int_out);
+    cudaFuncAttributes attr;
+    if (!k || cudaFuncGetAttributes(&attr, k) != cudaSuccess) return -1;
+    return attr.numRegs;
+}
+
+}  // namespace gemm

@@ -1,0 +1,79 @@
+// Internal declarations shared by the library's translation units (not part
+// of the public C ABI in include/dense_int8_matrix.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gemm {
+
+// ---- the tensor-core kernel family (gemm_tc.cu) ---------------------------
+// One CTA = 12 warps: warp 0 issues TMA copies, warp 1 owns TMEM and issues
+// tcgen05.mma, warps 2-3 idle, warps 4-11 drain the accumulator (epilogue).
+constexpr int kTcThreads = 384;
+constexpr int kTcStages = 4;         // operand ring depth
+constexpr int kTcBK = 64;            // K elements of a 16-bit operand per stage
+constexpr int kTcRowBytes = 128;     // kTcBK * 2: one 128-byte swizzle row
+constexpr int kTcEpilogueWarps = 8;
+
+// int8 problems run on f16 tensor-core MMAs with fp32 accumulation.  Every
+// int8 value and every product (|a*b| <= 2^14) is exact in f16 / fp32, and a
+// fp32 sum of integers is exact while its magnitude stays within 2^24, i.e.
+// for at most 2^24 / 2^14 = 1024 products.  So the accumulator is drained to
+// int32 registers (exact) after every kI8ChunkK elements of K.
+constexpr int kI8ChunkK = 1024;
+
+constexpr int tc_tmem_cols(int bn) {
+    int need = 2 * bn < 32 ? 32 : 2 * bn;
+    int cols = 32;
+    while (cols < need) cols *= 2;
+    return cols;
+}
+
+constexpr size_t tc_smem_bytes(int bm, int bn) {
+    // operand ring + 1 KiB to align it to the 1024-byte swizzle atom +
+    // 1 KiB for barriers and flags
+    return static_cast<size_t>(kTcStages) * (bm + bn) * kTcRowBytes + 1024 + 1024;
+}
+
+// Registers per thread the kernel is compiled for (launch bounds): wide
+// tiles keep 64-128 running sums per epilogue thread and run one CTA per SM;
+// narrow tiles fit two CTAs per SM.
+constexpr int tc_regs_per_thread(int bn) { return bn >= 128 ? 168 : 80; }
+constexpr int tc_min_blocks(int bn) { return bn >= 128 ? 1 : 2; }
+
+struct TcLaunch {
+    const void* A16;      // m x k_pitch 16-bit operand (f16 for int8 problems, bf16 otherwise)
+    const void* B16;      // n x k_pitch 16-bit operand
+    void* C;              // m x n int32 (int8 problems) or fp32
+    int* err;             // device error word
+    int64_t m, n, k, k_pitch;
+    int bm, bn;
+    int grid;
+    int chunk_kb;         // k-blocks accumulated in TMEM before a drain
+    bool int_out;         // true: int8 problem (f16 operands, int32 output)
+};
+
+cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream);
+// Occupancy of one kernel instance (CTAs per SM) as the runtime reports it.
+int tc_occupancy(int bm, int bn, bool int_out);
+int tc_num_regs(int bm, int bn, bool int_out);
+
+// ---- operand staging (stage.cu) --------------------------------------------
+// int8 -> f16 (exact), row pitch k -> k_pitch, for A (m rows) and Bt (n rows).
+cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
+                            int64_t n, int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream);
+// 16-bit copy with row pitch k -> k_pitch (bf16 problems whose k is not a
+// multiple of 8).
+cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
+                             int64_t n, int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream);
+
+// ---- skinny path (gemm_skinny.cu) -------------------------------------------
+cudaError_t launch_skinny_i8(const int8_t* A, const int8_t* Bt, int32_t* C, int64_t m, int64_t n, int64_t k,
+                             int num_sms, cudaStream_t stream);
+
+// ---- driver entry point for tensor-map encoding (gemm_tc.cu) ----------------
+bool tensor_map_encoder_available();
+
+}  // namespace gemm

@@ -1,0 +1,196 @@
+// Host tile selector: the five steps of patent CN114238853A
+// ("一種矩陣乘分片配置選擇方法及系統"), re-derived for the sm_103a tensor core.
+//
+//   claim 1 step 1 / claim 2  enumerate tiles the matrix unit can run: BM in
+//                             {64, 128} (M of one cta_group::1 MMA), BN in
+//                             {32, 64, 128, 256} (multiples of the minimum
+//                             N); K depth 64 16-bit elements per stage
+//   claim 3                   drop tiles whose shared memory or TMEM (two
+//                             accumulators of BN columns) exceed one SM
+//   claim 4 S1-S3             Thread_Blocks = output tiles; keep tiles with at
+//                             least one tile per SM; if none, the problem is
+//                             too small: keep only the smallest tile
+//   claim 5                   compute-to-memory ratio 2*BM*BN/((BM+BN)*2);
+//                             keep the largest
+//   claim 6                   block_per_cu from registers, shared memory and
+//                             TMEM; waves = ceil(tiles/(SMs*block_per_cu));
+//                             keep the fewest
+//   (unstated tie-break)      larger BM*BN, then larger BM
+//   claim 7                   every tile is a compiled template instance; the
+//                             plan names the one to launch
+// int8 problems with m <= 64 are routed to the skinny path first.
+#include <cstdint>
+
+#include "../../include/dense_int8_matrix.h"
+#include "internal.h"
+
+namespace gemm {
+
+namespace {
+
+constexpr int64_t kSmemPerCtaMax = 232448;
+constexpr int64_t kSmemPerSm = 233472;
+constexpr int64_t kRegsPerSm = 65536;
+constexpr int64_t kTmemColsPerSm = 512;
+constexpr int64_t kMaxDim = 2147483647;
+
+struct Tile {
+    int bm, bn;
+};
+constexpr Tile kTiles[] = {{64, 32}, {64, 64}, {64, 128}, {64, 256}, {128, 32}, {128, 64}, {128, 128}, {128, 256}};
+constexpr int kNumTiles = sizeof(kTiles) / sizeof(kTiles[0]);
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool tile_fits(const Tile& t) {
+    return static_cast<int64_t>(tc_smem_bytes(t.bm, t.bn)) <= kSmemPerCtaMax &&
+           static_cast<int64_t>(tc_tmem_cols(t.bn)) <= kTmemColsPerSm;
+}
+
+int64_t out_tiles(const Tile& t, int64_t m, int64_t n) { return ceil_div(m, t.bm) * ceil_div(n, t.bn); }
+
+double tile_ratio(const Tile& t) {
+    // flops of one K step over the bytes it stages: 2*BM*BN*BK / ((BM+BN)*BK*2)
+    return 2.0 * t.bm * t.bn / ((t.bm + t.bn) * 2.0);
+}
+
+int tile_bpc(const Tile& t) {
+    const int64_t by_regs = kRegsPerSm / (static_cast<int64_t>(kTcThreads) * tc_regs_per_thread(t.bn));
+    const int64_t by_smem = kSmemPerSm / static_cast<int64_t>(tc_smem_bytes(t.bm, t.bn));
+    const int64_t by_tmem = kTmemColsPerSm / tc_tmem_cols(t.bn);
+    int64_t b = by_regs;
+    if (by_smem < b) b = by_smem;
+    if (by_tmem < b) b = by_tmem;
+    return static_cast<int>(b);
+}
+
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+}  // namespace
+
+gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t num_sms, gemm_plan* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_DTYPE_I8 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    if (m < 1 || k < 1 || n < 1 || m > kMaxDim || k > kMaxDim || n > kMaxDim) return GEMM_ERR_INVALID_ARG;
+    if (num_sms < 1) return GEMM_ERR_INVALID_ARG;
+    if (dtype == GEMM_DTYPE_I8 && k > GEMM_I8_MAX_K) return GEMM_ERR_OVERFLOW_RISK;
+
+    gemm_plan p{};
+    p.version = GEMM_PLAN_VERSION;
+    p.dtype = dtype;
+    p.num_sms = num_sms;
+    p.m = m;
+    p.k = k;
+    p.n = n;
+
+    // Routing: a skinny int8 problem streams Bt once on CUDA cores.
+    if (dtype == GEMM_DTYPE_I8 && m <= 64) {
+        p.path = GEMM_PATH_SKINNY;
+        p.bm = static_cast<int32_t>(m);
+        p.bn = 32;
+        p.bk = 16;
+        p.stages = 1;
+        const int64_t tiles = ceil_div(n, 32);
+        if (tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
+        p.tiles = static_cast<int32_t>(tiles);
+        p.grid = p.tiles;
+        p.bpc = 0;
+        p.waves = 0;
+        p.k_pitch = static_cast<int32_t>(k);
+        p.chunk_k = static_cast<int32_t>(k);
+        p.ratio = 2.0 * m / (m + 1.0);  // flops per byte streamed (m rows of A reused per Bt byte)
+        p.workspace_bytes = 0;
+        *out = p;
+        return GEMM_OK;
+    }
+
+    // Step 1: candidates; step 2: resource fit.
+    bool alive[kNumTiles];
+    for (int i = 0; i < kNumTiles; ++i) alive[i] = tile_fits(kTiles[i]);
+
+    // Step 3: keep tiles that fill every SM with at least one output tile.
+    bool any_full = false;
+    for (int i = 0; i < kNumTiles; ++i)
+        if (alive[i] && out_tiles(kTiles[i], m, n) >= num_sms) any_full = true;
+    if (any_full) {
+        for (int i = 0; i < kNumTiles; ++i)
+            if (alive[i] && out_tiles(kTiles[i], m, n) < num_sms) alive[i] = false;
+    } else {
+        // Too small to fill the chip: only the smallest tile stays.
+        int smallest = -1;
+        for (int i = 0; i < kNumTiles; ++i) {
+            if (!alive[i]) continue;
+            if (smallest < 0) {
+                smallest = i;
+                continue;
+            }
+            const Tile& a = kTiles[i];
+            const Tile& b = kTiles[smallest];
+            const int64_t aa = static_cast<int64_t>(a.bm) * a.bn, bb = static_cast<int64_t>(b.bm) * b.bn;
+            if (aa < bb || (aa == bb && a.bm < b.bm)) smallest = i;
+        }
+        for (int i = 0; i < kNumTiles; ++i) alive[i] = (i == smallest);
+        p.fallback = 1;
+    }
+
+    // Step 4: largest compute-to-memory ratio.
+    double best_ratio = -1.0;
+    for (int i = 0; i < kNumTiles; ++i)
+        if (alive[i] && tile_ratio(kTiles[i]) > best_ratio) best_ratio = tile_ratio(kTiles[i]);
+    for (int i = 0; i < kNumTiles; ++i)
+        if (alive[i] && tile_ratio(kTiles[i]) != best_ratio) alive[i] = false;
+
+    // Step 5: fewest waves; then the tie-break.
+    int best = -1;
+    int64_t best_waves = 0;
+    for (int i = 0; i < kNumTiles; ++i) {
+        if (!alive[i]) continue;
+        const Tile& t = kTiles[i];
+        const int64_t w = ceil_div(out_tiles(t, m, n), static_cast<int64_t>(num_sms) * tile_bpc(t));
+        bool take = false;
+        if (best < 0 || w < best_waves) {
+            take = true;
+        } else if (w == best_waves) {
+            const Tile& b = kTiles[best];
+            const int64_t ta = static_cast<int64_t>(t.bm) * t.bn, tb = static_cast<int64_t>(b.bm) * b.bn;
+            take = ta > tb || (ta == tb && t.bm > b.bm);
+        }
+        if (take) {
+            best = i;
+            best_waves = w;
+        }
+    }
+    if (best < 0) return GEMM_ERR_INVALID_ARG;
+    const Tile& t = kTiles[best];
+    const int64_t tiles = out_tiles(t, m, n);
+    if (tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
+    const int bpc = tile_bpc(t);
+
+    p.path = GEMM_PATH_TENSOR;
+    p.bm = t.bm;
+    p.bn = t.bn;
+    p.bk = kTcBK;
+    p.stages = kTcStages;
+    p.tiles = static_cast<int32_t>(tiles);
+    p.bpc = bpc;
+    const int64_t slots = static_cast<int64_t>(num_sms) * bpc;
+    p.grid = static_cast<int32_t>(tiles < slots ? tiles : slots);
+    p.waves = static_cast<int32_t>(best_waves);
+    p.ratio = tile_ratio(t);
+    // Staged 16-bit rows need a 16-byte pitch for TMA.
+    const int64_t k_pitch = round_up(k, 8);
+    if (k_pitch > kMaxDim) return GEMM_ERR_INVALID_ARG;
+    p.k_pitch = static_cast<int32_t>(k_pitch);
+    const int64_t num_kb = ceil_div(k, kTcBK);
+    if (dtype == GEMM_DTYPE_I8) {
+        p.chunk_k = kI8ChunkK;
+        p.workspace_bytes = round_up(m * k_pitch * 2, 256) + round_up(n * k_pitch * 2, 256);
+    } else {
+        p.chunk_k = static_cast<int32_t>(num_kb * kTcBK > kMaxDim ? kMaxDim : num_kb * kTcBK);
+        p.workspace_bytes = (k % 8 == 0) ? 0 : round_up(m * k_pitch * 2, 256) + round_up(n * k_pitch * 2, 256);
+    }
+    *out = p;
+    return GEMM_OK;
+}
+
+}  // namespace gemm

@@ -1,0 +1,136 @@
+// Operand staging for the tensor-core path.
+//
+// sm_103a has no integer tensor-core MMA (ptxas rejects tcgen05.mma
+// .kind::i8 for this target), so int8 operands are widened to f16, in which
+// every int8 value is exact, and multiplied on the f16 tensor cores.  The
+// same pass re-pitches rows whose length is not a multiple of 16 bytes, which
+// TMA requires of every row pitch; the pad is never read (the tensor map's K
+// extent is k, so TMA fills K beyond it with zeros).
+//
+// int8 -> f16 without a conversion instruction: for a byte x, the f16 bit
+// pattern 0x6400 | (x ^ 0x80) encodes 1024 + (x + 128); subtracting 1152 (exact
+// in f16) leaves x.  Memory-bound: 1 byte read and 2 written per element.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace gemm {
+
+namespace {
+
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t biased_word, uint32_t selector) {
+    // two bytes of the biased word become the low bytes of two f16 values
+    // whose high bytes are 0x64
+    const uint32_t packed = __byte_perm(biased_word, 0x64646464u, selector);
+    __half2 h = *reinterpret_cast<const __half2*>(&packed);
+    const __half2 offset = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    h = __hsub2(h, offset);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Contiguous rows (k == k_pitch, k % 16 == 0): 16 int8 -> 16 f16 per item.
+__global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restrict__ srcA,
+                                                            const uint4* __restrict__ srcB, uint4* __restrict__ dstA,
+                                                            uint4* __restrict__ dstB, int64_t itemsA,
+                                                            int64_t itemsB) {
+    const int64_t total = itemsA + itemsB;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const bool isA = i < itemsA;
+        const int64_t j = isA ? i : i - itemsA;
+        const uint4 v = ld_stream((isA ? srcA : srcB) + j);
+        const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+        uint4 lo, hi;
+        lo.x = i8x2_to_f16x2(w[0], 0x4140u);
+        lo.y = i8x2_to_f16x2(w[0], 0x4342u);
+        lo.z = i8x2_to_f16x2(w[1], 0x4140u);
+        lo.w = i8x2_to_f16x2(w[1], 0x4342u);
+        hi.x = i8x2_to_f16x2(w[2], 0x4140u);
+        hi.y = i8x2_to_f16x2(w[2], 0x4342u);
+        hi.z = i8x2_to_f16x2(w[3], 0x4140u);
+        hi.w = i8x2_to_f16x2(w[3], 0x4342u);
+        uint4* d = (isA ? dstA : dstB) + 2 * j;
+        d[0] = lo;
+        d[1] = hi;
+    }
+}
+
+// Any k: one element per item, rows re-pitched to k_pitch.
+__global__ void __launch_bounds__(256) stage_i8_rows_kernel(const int8_t* __restrict__ A,
+                                                            const int8_t* __restrict__ Bt, __half* __restrict__ Ah,
+                                                            __half* __restrict__ Bh, int64_t m, int64_t n, int64_t k,
+                                                            int64_t k_pitch) {
+    const int64_t totalA = m * k;
+    const int64_t total = totalA + n * k;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const bool isA = i < totalA;
+        const int64_t j = isA ? i : i - totalA;
+        const int64_t row = j / k, col = j - row * k;
+        const int8_t x = (isA ? A : Bt)[j];
+        (isA ? Ah : Bh)[row * k_pitch + col] = __short2half_rn(static_cast<short>(x));
+    }
+}
+
+// 16-bit copy with re-pitched rows.
+__global__ void __launch_bounds__(256) stage_b16_rows_kernel(const uint16_t* __restrict__ A,
+                                                             const uint16_t* __restrict__ Bt,
+                                                             uint16_t* __restrict__ Ah, uint16_t* __restrict__ Bh,
+                                                             int64_t m, int64_t n, int64_t k, int64_t k_pitch) {
+    const int64_t totalA = m * k;
+    const int64_t total = totalA + n * k;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const bool isA = i < totalA;
+        const int64_t j = isA ? i : i - totalA;
+        const int64_t row = j / k, col = j - row * k;
+        (isA ? Ah : Bh)[row * k_pitch + col] = (isA ? A : Bt)[j];
+    }
+}
+
+int grid_for(int64_t items, int num_sms) {
+    // 8 resident 256-thread blocks per SM, grid a multiple of the SM count
+    int64_t want = (items + 255) / 256;
+    int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (want > cap) want = cap;
+    if (want < 1) want = 1;
+    return static_cast<int>(want);
+}
+
+}  // namespace
+
+cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m, int64_t n,
+                            int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream) {
+    const bool aligned = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bt) |
+                           reinterpret_cast<uintptr_t>(Ah) | reinterpret_cast<uintptr_t>(Bh)) &
+                          15u) == 0;
+    if (k == k_pitch && (k % 16) == 0 && aligned) {
+        const int64_t itemsA = m * k / 16, itemsB = n * k / 16;
+        stage_i8_flat_kernel<<<grid_for(itemsA + itemsB, num_sms), 256, 0, stream>>>(
+            reinterpret_cast<const uint4*>(A), reinterpret_cast<const uint4*>(Bt), reinterpret_cast<uint4*>(Ah),
+            reinterpret_cast<uint4*>(Bh), itemsA, itemsB);
+    } else {
+        stage_i8_rows_kernel<<<grid_for((m + n) * k, num_sms), 256, 0, stream>>>(
+            A, Bt, reinterpret_cast<__half*>(Ah), reinterpret_cast<__half*>(Bh), m, n, k, k_pitch);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
+                             int64_t n, int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream) {
+    stage_b16_rows_kernel<<<grid_for((m + n) * k, num_sms), 256, 0, stream>>>(A, Bt, Ah, Bh, m, n, k, k_pitch);
+    return cudaGetLastError();
+}
+
+}  // namespace gemm

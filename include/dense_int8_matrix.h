@@ -1,0 +1,176 @@
+/*
+ * dense_int8_matrix: dense matrix multiply C = A x B on one NVIDIA GB300
+ * (sm_103a).  C ABI of libgemm_gb300.so.
+ *
+ * The operation is the one the TPU's 256x256 INT8 multiply-accumulate array
+ * evaluates ("文章导读: Motivation for and Evaluation of the First Tensor
+ * Processing Unit", sections "TPU介绍" and "TPU使用的技术"):
+ *
+ *     C[i][j] = sum_{kk < k} A[i][kk] * B[kk][j]
+ *
+ * in two forms: int8 x int8 -> int32 (exact) and bf16 x bf16 -> fp32
+ * (fp32 accumulation).  The tile configuration of each problem is chosen on
+ * the host by the five-step method of patent CN114238853A
+ * ("一種矩陣乘分片配置選擇方法及系統", claims 1-7), re-derived for sm_103a.
+ *
+ * Layout (all operands dense, leading dimensions implied):
+ *   A   m x k row-major              A[i][kk] = A[i*k + kk]
+ *   Bt  n x k row-major: B stored K-major (transposed), B[kk][j] = Bt[j*k + kk]
+ *   C   m x n row-major              C[i][j]  = C[i*n + j]
+ *
+ * Ownership: the caller owns every buffer.  The library never frees caller
+ * memory.  Device scratch (the f16 copies of int8 operands) is taken from a
+ * private stream-ordered memory pool inside gemm_*_run and returned to it on
+ * the same stream.  A plan is plain data: copy it freely, nothing to free.
+ *
+ * Asynchrony: gemm_*_run only enqueues work on `stream` (a cudaStream_t;
+ * NULL = the legacy default stream) and returns.  Launch errors are returned
+ * as GEMM_ERR_CUDA.  Errors found while kernels run (a wait that ran past its
+ * time limit) are reported by gemm_device_error().
+ *
+ * Thread safety: every entry point may be called from several host threads.
+ */
+#ifndef DENSE_INT8_MATRIX_H
+#define DENSE_INT8_MATRIX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* null pointer, size out of range, bad plan */
+    GEMM_ERR_MISALIGNED = 2,         /* A or Bt not 16-byte aligned, C not 4-byte aligned */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 */
+    GEMM_ERR_CUDA = 4,               /* a CUDA runtime call failed */
+    GEMM_ERR_OVERFLOW_RISK = 5,      /* int8: k > 131071, so |C| could exceed int32 */
+    GEMM_ERR_TIMEOUT = 6             /* a kernel wait ran past its limit (see gemm_device_error) */
+} gemm_status;
+
+enum { GEMM_PATH_TENSOR = 0, GEMM_PATH_SKINNY = 1 };
+enum { GEMM_DTYPE_I8 = 0, GEMM_DTYPE_BF16 = 1 };
+
+/* Kernel kinds counted by the trace (gemm_trace_*). */
+enum {
+    GEMM_KERNEL_STAGE = 0,  /* operand staging: int8 -> f16 widening / re-pitching */
+    GEMM_KERNEL_TC = 1,     /* tcgen05 tensor-core GEMM */
+    GEMM_KERNEL_SKINNY = 2, /* skinny-m GEMM */
+    GEMM_KERNEL_KINDS = 3
+};
+
+#define GEMM_PLAN_VERSION 1
+#define GEMM_I8_MAX_K 131071 /* 131071 * 128 * 128 < 2^31 */
+
+/*
+ * The selected configuration (patent CN114238853A claim 7: "input the size,
+ * select the configuration and its kernel, run").  Filled by gemm_*_plan.
+ */
+typedef struct gemm_plan {
+    int32_t version;   /* GEMM_PLAN_VERSION */
+    int32_t path;      /* GEMM_PATH_* */
+    int32_t dtype;     /* GEMM_DTYPE_* */
+    int32_t num_sms;   /* SM count the plan was made for */
+    int64_t m, k, n;
+    int32_t bm, bn, bk;  /* CTA tile; bk = K elements per pipeline stage */
+    int32_t stages;      /* depth of the shared-memory operand ring */
+    int32_t tiles;       /* output tiles: Thread_Blocks of claim 4 */
+    int32_t bpc;         /* CTAs per SM: block_per_cu of claim 6 */
+    int32_t grid;        /* CTAs launched (persistent): min(tiles, num_sms * bpc) */
+    int32_t waves;       /* ceil(tiles / (num_sms * bpc)): Launch_kernel_times of claim 6 */
+    int32_t k_pitch;     /* row pitch (elements) of the staged 16-bit operands */
+    int32_t chunk_k;     /* K elements accumulated in fp32 before an exact int32 drain */
+    int32_t fallback;    /* 1 if no tile filled the chip (claim 4 S3) */
+    int32_t reserved0;
+    double ratio;        /* compute-to-memory ratio of the tile (claim 5), flop per byte */
+    int64_t workspace_bytes; /* device scratch gemm_*_run takes from its pool */
+    int64_t reserved[4];
+} gemm_plan;
+
+/*
+ * Plan an int8 problem (m x k) x (k x n) for the current CUDA device.
+ * Routing: m <= 64 -> skinny path (streams Bt once); otherwise the five
+ * steps of CN114238853A claim 1 select a (BM, BN) tile.  Host-only apart from
+ * one cached query of the device's SM count.
+ * Errors: GEMM_ERR_INVALID_ARG (out == NULL, m/k/n outside [1, 2^31-1]),
+ * GEMM_ERR_OVERFLOW_RISK (k > GEMM_I8_MAX_K), GEMM_ERR_CUDA (no device).
+ */
+gemm_status gemm_i8_plan(int64_t m, int64_t k, int64_t n, gemm_plan *out);
+
+/* Plan a bf16 problem for the current device (always the tensor-core path). */
+gemm_status gemm_bf16_plan(int64_t m, int64_t k, int64_t n, gemm_plan *out);
+
+/*
+ * Pure host planner: the same selection for an explicit SM count, with no
+ * CUDA call at all.  dtype is GEMM_DTYPE_*.  Same errors as the above.
+ */
+gemm_status gemm_plan_for_sms(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t num_sms,
+                              gemm_plan *out);
+
+/*
+ * C (int32, m x n) = A (int8, m x k) x B, with B given as Bt (int8, n x k).
+ * All pointers are device pointers on the current device.  A and Bt must be
+ * 16-byte aligned, C 4-byte aligned.  Exact: every element equals the int64
+ * sum, which the plan's k limit keeps inside int32.
+ * A plan may be edited before the call to force another compiled tile (bm in
+ * {64, 128}, bn in {32, 64, 128, 256}) or another grid size (>= 1); every
+ * such choice gives the same result.
+ * Errors: GEMM_ERR_INVALID_ARG (null pointer, plan not from gemm_i8_plan or
+ * of another version, tile not compiled), GEMM_ERR_MISALIGNED,
+ * GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_CUDA.  Nothing is launched when an
+ * error is returned.
+ */
+gemm_status gemm_i8_run(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
+                        void *stream);
+
+/*
+ * C (fp32, m x n) = A (bf16, m x k) x B, B given as Bt (bf16, n x k); bf16
+ * values are passed as their 16-bit patterns.  fp32 accumulation:
+ * |C - exact| <= 1e-3 * sum_k |a*b| elementwise.  Same rules and errors as
+ * gemm_i8_run.
+ */
+gemm_status gemm_bf16_run(const gemm_plan *plan, const uint16_t *A, const uint16_t *Bt, float *C,
+                          void *stream);
+
+/*
+ * End-to-end forms: A, Bt and C are HOST pointers (pinned or pageable).  The
+ * call takes device buffers from the library's pool, copies A and Bt to the
+ * device, runs the plan, copies C back and waits for `stream` to finish, so
+ * C is ready when it returns.
+ */
+gemm_status gemm_i8_run_host(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
+                             void *stream);
+gemm_status gemm_bf16_run_host(const gemm_plan *plan, const uint16_t *A, const uint16_t *Bt, float *C,
+                               void *stream);
+
+/*
+ * Waits for `stream`, then reads and clears the current device's error word.
+ * Returns GEMM_OK, GEMM_ERR_TIMEOUT (a kernel wait ran past its 2 s limit
+ * and the kernel returned early; *code gets the stage that gave up) or
+ * GEMM_ERR_CUDA.  `code` may be NULL.
+ */
+gemm_status gemm_device_error(void *stream, int32_t *code);
+
+/*
+ * Tracing: while enabled, every kernel launch made by gemm_*_run records a
+ * pair of CUDA events around itself on the launch stream (at most
+ * `capacity` launches are recorded).  gemm_trace_collect waits for them and
+ * writes, per GEMM_KERNEL_* kind, the summed device time in ms and the
+ * launch count (arrays of GEMM_KERNEL_KINDS entries), then disables tracing.
+ */
+gemm_status gemm_trace_begin(int32_t capacity);
+gemm_status gemm_trace_collect(float *ms_per_kind, int32_t *launches_per_kind);
+
+/* Registers per thread and CTAs per SM of the compiled tensor-core kernel for
+ * a tile (-1 / 0 if no such kernel); needs a device. */
+gemm_status gemm_tc_kernel_info(int32_t bm, int32_t bn, int32_t dtype, int32_t *regs, int32_t *ctas_per_sm);
+
+/* Human-readable name of a status. */
+const char *gemm_status_string(gemm_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_INT8_MATRIX_H */

@@ -1,0 +1,258 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+int8 results must be bit-exact; bf16 results must satisfy
+|C - oracle| <= 1e-3 * sum_k |a*b| elementwise.  Full comparisons at sizes
+the oracle finishes in seconds; at the full 8192^3 sizes, sampled entries
+computed one by one by the oracle plus (int8) the Freivalds identity
+C r = A (B r), exact in float64 at these magnitudes."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_int8_matrix_gb300 import binding as B
+from dense_int8_matrix_gb300 import workloads
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_int8_matrix_gb300 import build
+    build.build()
+    oracle.build()
+    B.load()
+    yield
+    st, code = B.gemm_device_error()
+    assert st == B.GEMM_OK, "device error word set: code %d" % code
+
+
+# ------------------------------------------------------ named workloads ----
+
+def test_workload_i8_256():
+    A, Bt = workloads.make_inputs("i8_256", (256, 256, 256))
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
+
+
+def test_workload_i8_4096():
+    A, Bt = workloads.make_inputs("i8_4096", (4096, 4096, 4096))
+    C = G.gpu_i8(A, Bt)
+    G.assert_i8_exact(A, Bt, C)
+
+
+@pytest.mark.parametrize("m", [1, 8, 16, 32, 64, 128])
+def test_workload_i8_skinny(m):
+    A, Bt = workloads.make_inputs("i8_skinny", (m, 8192, 8192))
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
+
+
+@pytest.mark.parametrize("shape", [(1000, 777, 3000), (4097, 16384, 255)])
+def test_workload_i8_ragged_full(shape):
+    A, Bt = workloads.make_inputs("i8_ragged", shape)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
+
+
+def test_workload_i8_ragged_8192_sampled():
+    shape = (8192, 8192, 8192)
+    A, Bt = workloads.make_inputs("i8_ragged", shape)
+    C = G.gpu_i8(A, Bt)
+    rows, cols = G.sample_positions(8192, 8192, 8192, seed=1)
+    want = oracle.gemm_i8_entries(A.numpy(), Bt.numpy(), rows, cols)
+    got = C.numpy()[rows, cols].astype(np.int64)
+    assert np.array_equal(got, want)
+    # two complete rows and columns
+    for r in (0, 8191):
+        ref = oracle.gemm_i8(A[r:r + 1].numpy(), Bt.numpy())
+        assert np.array_equal(C[r:r + 1].numpy(), ref)
+    for c in (5, 8190):
+        ref = oracle.gemm_i8(A.numpy(), Bt[c:c + 1].numpy())
+        assert np.array_equal(C[:, c:c + 1].numpy(), ref)
+    G.freivalds_i8(A, Bt, C)
+
+
+def test_workload_bf16_8192_sampled():
+    shape = (8192, 8192, 8192)
+    A, Bt = workloads.make_inputs("bf16_8192", shape)
+    C = G.gpu_bf16(A, Bt)
+    rows, cols = G.sample_positions(8192, 8192, 8192, seed=2)
+    s, sa = oracle.gemm_bf16_entries(G.bits(A), G.bits(Bt), rows, cols)
+    got = C.numpy()[rows, cols].astype(np.float64)
+    assert np.all(np.abs(got - s) <= 1e-3 * sa)
+    ref, S = oracle.gemm_bf16(G.bits(A[:2]), G.bits(Bt))
+    assert np.all(np.abs(C[:2].numpy().astype(np.float64) - ref) <= 1e-3 * S)
+    assert np.isfinite(C.numpy()).all()
+
+
+# -------------------------------------------------- every compiled tile ----
+
+TILES = [(bm, bn) for bm in (64, 128) for bn in (32, 64, 128, 256)]
+
+
+def forced_plan(dtype, m, k, n, bm, bn, grid):
+    p = B.gemm_plan_for_sms(dtype, m, k, n, torch.cuda.get_device_properties(0).multi_processor_count)
+    p.bm, p.bn, p.grid = bm, bn, grid
+    return p
+
+
+@pytest.mark.parametrize("bm,bn", TILES)
+@pytest.mark.parametrize("grid", [3, 1000])
+def test_i8_every_tile(bm, bn, grid):
+    # several tiles in both directions plus ragged tails; k = 2100 runs two
+    # full 1024-element accumulator chunks and a ragged third one
+    m, k, n = 300, 2100, 700
+    A = workloads.random_i8((m, k), 101)
+    Bt = workloads.random_i8((n, k), 102)
+    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, bm, bn, grid)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt, plan=p))
+
+
+@pytest.mark.parametrize("bm,bn", TILES)
+def test_bf16_every_tile(bm, bn):
+    m, k, n = 300, 1000, 700
+    A = workloads.random_bf16((m, k), 103)
+    Bt = workloads.random_bf16((n, k), 104)
+    p = forced_plan(B.GEMM_DTYPE_BF16, m, k, n, bm, bn, 5)
+    G.assert_bf16_close(A, Bt, G.gpu_bf16(A, Bt, plan=p))
+
+
+# ------------------------------------------------------------ edge cases ----
+
+@pytest.mark.parametrize("m,k,n", [
+    (65, 1, 1), (65, 7, 3), (129, 63, 33), (200, 64, 64), (200, 65, 129),
+    (130, 1024, 130), (130, 1025, 130), (257, 2048, 100), (300, 3073, 257),
+    (1, 1, 1), (64, 16, 16), (63, 1000, 500), (8, 4100, 77), (2, 17, 5),
+    (128, 8, 255), (513, 520, 1001),
+])
+def test_i8_edge_shapes(m, k, n):
+    A = workloads.random_i8((m, k), m * 7 + k)
+    Bt = workloads.random_i8((n, k), n * 11 + k)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
+
+
+@pytest.mark.parametrize("m,k,n", [(200, 1001, 300), (129, 8, 65), (65, 12, 40), (1, 64, 1)])
+def test_bf16_edge_shapes(m, k, n):
+    A = workloads.random_bf16((m, k), m + 3 * k)
+    Bt = workloads.random_bf16((n, k), n + 5 * k)
+    G.assert_bf16_close(A, Bt, G.gpu_bf16(A, Bt))
+
+
+@pytest.mark.parametrize("m", [32, 200])
+def test_i8_extreme_values_exact(m):
+    # all -128: every fp32 chunk of 1024 products reaches exactly 2^24; the
+    # int32 result 16384 * k is exact only if the chunked drain works
+    k, n = 16384, 160
+    A = torch.full((m, k), -128, dtype=torch.int8)
+    Bt = torch.full((n, k), -128, dtype=torch.int8)
+    C = G.gpu_i8(A, Bt)
+    assert torch.all(C == 16384 * k)
+
+
+def test_i8_max_k_exact():
+    # k = 131071: the largest k the library accepts; C = 131071 * 16384
+    m, k, n = 130, 131071, 40
+    A = torch.full((m, k), -128, dtype=torch.int8)
+    Bt = torch.full((n, k), -128, dtype=torch.int8)
+    Bt[1::2] = 127
+    C = G.gpu_i8(A, Bt)
+    assert torch.all(C[:, 0::2] == 131071 * 16384)
+    assert torch.all(C[:, 1::2] == -131071 * 16256)
+
+
+def test_i8_alternating_signs_large_k():
+    m, k, n = 256, 16384, 256
+    A = workloads.random_i8((m, k), 5)
+    sign = torch.where(torch.arange(k) % 2 == 0, 1, -1).to(torch.int8)
+    A = torch.where(A == -128, torch.tensor(-127, dtype=torch.int8), A)
+    Bt = (A[:n] * sign).to(torch.int8)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
+
+
+def test_bf16_integer_inputs_exact():
+    # integer bf16 inputs with small sums: fp32 accumulation is exact
+    m, k, n = 300, 2000, 260
+    Ai = workloads.random_i8((m, k), 8, -16, 16)
+    Bi = workloads.random_i8((n, k), 9, -16, 16)
+    C = G.gpu_bf16(Ai.float().to(torch.bfloat16), Bi.float().to(torch.bfloat16))
+    ref = oracle.gemm_i8(Ai.numpy(), Bi.numpy())
+    assert np.array_equal(C.numpy(), ref.astype(np.float32))
+
+
+# --------------------------------------------------------- ABI behaviour ----
+
+def test_run_on_side_stream_and_repeat():
+    m, k, n = 700, 3000, 500
+    A = workloads.random_i8((m, k), 21)
+    Bt = workloads.random_i8((n, k), 22)
+    s = torch.cuda.Stream()
+    dA, dB = A.cuda(), Bt.cuda()
+    p = B.gemm_i8_plan(m, k, n)
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            C = torch.empty((m, n), dtype=torch.int32, device="cuda")
+            B.gemm_i8_run(p, dA, dB, C, s)
+            outs.append(C)
+    s.synchronize()
+    ref = oracle.gemm_i8(A.numpy(), Bt.numpy())
+    for C in outs:
+        assert np.array_equal(C.cpu().numpy(), ref)
+
+
+def test_host_entry_points():
+    m, k, n = 300, 1000, 200
+    A = workloads.random_i8((m, k), 23)
+    Bt = workloads.random_i8((n, k), 24)
+    C = torch.empty((m, n), dtype=torch.int32).pin_memory()
+    B.gemm_i8_run_host(B.gemm_i8_plan(m, k, n), A.pin_memory(), Bt.pin_memory(), C)
+    G.assert_i8_exact(A, Bt, C)
+    Ab = workloads.random_bf16((m, k), 25)
+    Bb = workloads.random_bf16((n, k), 26)
+    Cb = torch.empty((m, n), dtype=torch.float32)
+    B.gemm_bf16_run_host(B.gemm_bf16_plan(m, k, n), Ab, Bb, Cb)
+    G.assert_bf16_close(Ab, Bb, Cb)
+
+
+def test_misaligned_device_pointers_rejected():
+    lib = B.load()
+    buf = torch.zeros(4096, dtype=torch.int8, device="cuda")
+    p = B.gemm_i8_plan(128, 16, 16)
+    base = buf.data_ptr()
+    assert lib.gemm_i8_run(ctypes.byref(p), base + 1, base, base, None) == B.GEMM_ERR_MISALIGNED
+    assert lib.gemm_i8_run(ctypes.byref(p), base, base + 8, base, None) == B.GEMM_ERR_MISALIGNED
+
+
+def test_trace_counts_launches():
+    m, k, n = 512, 512, 512
+    dA = workloads.random_i8((m, k), 27).cuda()
+    dB = workloads.random_i8((n, k), 28).cuda()
+    C = torch.empty((m, n), dtype=torch.int32, device="cuda")
+    p = B.gemm_i8_plan(m, k, n)
+    B.gemm_trace_begin(16)
+    for _ in range(3):
+        B.gemm_i8_run(p, dA, dB, C)
+    ms, cnt = B.gemm_trace_collect()
+    assert cnt[B.GEMM_KERNEL_STAGE] == 3 and cnt[B.GEMM_KERNEL_TC] == 3
+    assert ms[B.GEMM_KERNEL_TC] > 0
+    ps = B.gemm_i8_plan(16, k, n)
+    B.gemm_trace_begin(4)
+    B.gemm_i8_run(ps, dA[:16].contiguous(), dB, C[:16].contiguous())
+    ms, cnt = B.gemm_trace_collect()
+    assert cnt == [0, 0, 1]
+
+
+@pytest.mark.parametrize("bm,bn", TILES)
+def test_kernel_resources_match_planner(bm, bn):
+    # the planner assumes these register counts (block_per_cu of claim 6);
+    # the compiled kernels must not use more, nor fit fewer CTAs per SM
+    assumed = 168 if bn >= 128 else 80
+    want_bpc = min(65536 // (384 * assumed), 233472 // (4 * (bm + bn) * 128 + 2048), 512 // (2 * bn))
+    for dtype in (B.GEMM_DTYPE_I8, B.GEMM_DTYPE_BF16):
+        regs, occ = B.gemm_tc_kernel_info(bm, bn, dtype)
+        assert 0 < regs <= assumed
+        assert occ >= want_bpc
