@@ -37,7 +37,7 @@ GEMM_I8_MAX_K = 131071
 EXPORTED = (
     "gemm_i8_plan", "gemm_bf16_plan", "gemm_plan_for_sms", "gemm_i8_run", "gemm_bf16_run",
     "gemm_i8_run_host", "gemm_bf16_run_host", "gemm_device_error", "gemm_trace_begin",
-    "gemm_trace_collect", "gemm_tc_kernel_info", "gemm_status_string",
+    "gemm_trace_collect", "gemm_tc_kernel_info", "gemm_selftest_wait_timeout", "gemm_status_string",
 )
 
 
@@ -103,6 +103,7 @@ def load():
         "gemm_trace_begin": [i32],
         "gemm_trace_collect": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)],
         "gemm_tc_kernel_info": [i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
+        "gemm_selftest_wait_timeout": [i32, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -236,6 +237,10 @@ def gemm_tc_kernel_info(bm: int, bn: int, dtype: int):
     _check(load().gemm_tc_kernel_info(bm, bn, dtype, ctypes.byref(regs), ctypes.byref(occ)),
            "gemm_tc_kernel_info")
     return regs.value, occ.value
+
+
+def gemm_selftest_wait_timeout(timeout_us: int, stream=None) -> None:
+    _check(load().gemm_selftest_wait_timeout(timeout_us, _stream(stream)), "gemm_selftest_wait_timeout")
 
 
 # ------------------------------------------------------------ convenience --

@@ -335,6 +335,18 @@ gemm_status gemm_tc_kernel_info(int32_t bm, int32_t bn, int32_t dtype, int32_t* 
     return *regs < 0 ? GEMM_ERR_INVALID_ARG : GEMM_OK;
 }
 
+gemm_status gemm_selftest_wait_timeout(int32_t timeout_us, void* stream) {
+    if (timeout_us < 1 || timeout_us > 2000000) return GEMM_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    gemm_status st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    if (!ds->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    if (launch_selftest_wait(ds->err_word, static_cast<uint64_t>(timeout_us) * 1000u,
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
 const char* gemm_status_string(gemm_status s) {
     switch (s) {
         case GEMM_OK: return "GEMM_OK";

@@ -321,12 +321,20 @@ bool encode_operand_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t
     return r == CUDA_SUCCESS;
 }
 
+// Opt in to the kernel's dynamic shared memory and ask for the largest
+// shared-memory carveout, so that the CTAs per SM the planner counts on fit.
+cudaError_t configure_kernel(const void* kern, size_t smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
 template <int BM, int BN, bool INT_OUT>
 cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     using Cfg = TcCfg<BM, BN>;
     auto kern = gemm_tc_kernel<BM, BN, INT_OUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::SMEM));
+    cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;
     CUtensorMap mA, mB;
     if (!encode_operand_map(&mA, a.A16, a.m, a.k, a.k_pitch, BM)) return cudaErrorInvalidValue;
@@ -394,9 +402,7 @@ int tc_occupancy(int bm, int bn, bool int_out) {
     const void* k = find_kernel(bm, bn, int_out);
     if (!k) return 0;
     const size_t smem = tc_smem_bytes(bm, bn);
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
-        return 0;
+    if (configure_kernel(k, smem) != cudaSuccess) return 0;
     int blocks = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, kTcThreads, smem) != cudaSuccess) return 0;
     return blocks;

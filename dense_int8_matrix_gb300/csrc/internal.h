@@ -73,6 +73,11 @@ cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah
 cudaError_t launch_skinny_i8(const int8_t* A, const int8_t* Bt, int32_t* C, int64_t m, int64_t n, int64_t k,
                              int num_sms, cudaStream_t stream);
 
+// ---- failure-detection self-test (selftest.cu) ------------------------------
+// One CTA waits on an mbarrier that nothing completes; the bounded wait gives
+// up after timeout_ns and records kDevErrTimeoutSelfTest in *err.
+cudaError_t launch_selftest_wait(int* err, uint64_t timeout_ns, cudaStream_t stream);
+
 // ---- driver entry point for tensor-map encoding (gemm_tc.cu) ----------------
 bool tensor_map_encoder_available();
 

@@ -19,6 +19,7 @@ enum DeviceErrorCode : int {
     kDevErrTimeoutMma = 2,        // MMA issuer waited too long for operands / accumulator
     kDevErrTimeoutEpilogue = 3,   // epilogue waited too long for an accumulator
     kDevErrTimeoutTeardown = 4,   // teardown waited too long for in-flight copies / MMAs
+    kDevErrTimeoutSelfTest = 5,   // the self-test's wait on a barrier nothing completes
 };
 
 // One wait gives up after this many nanoseconds of %globaltimer time, or after
@@ -76,14 +77,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // wait runs past its limit; in the latter case raises the flag and records
 // `code` in the device error word.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                             int* err_word, int code) {
+                                             int* err_word, int code, uint64_t timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it < kWaitIterCap; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (abort_flag != nullptr && *abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+            if (global_timer_ns() - t0 > timeout_ns) break;
         }
     }
     if (abort_flag != nullptr) *abort_flag = 1u;

@@ -166,6 +166,16 @@ gemm_status gemm_trace_collect(float *ms_per_kind, int32_t *launches_per_kind);
  * a tile (-1 / 0 if no such kernel); needs a device. */
 gemm_status gemm_tc_kernel_info(int32_t bm, int32_t bn, int32_t dtype, int32_t *regs, int32_t *ctas_per_sm);
 
+/*
+ * Failure-detection self-test.  Launches one CTA that waits on a barrier
+ * nothing completes, with a limit of `timeout_us` microseconds (1 .. 2e6)
+ * instead of the kernels' 2 s.  The wait gives up, records code 5 in the
+ * device error word and the kernel returns: a following gemm_device_error()
+ * returns GEMM_ERR_TIMEOUT with *code = 5, and the CUDA context stays usable.
+ * Nothing faults, traps or hangs.
+ */
+gemm_status gemm_selftest_wait_timeout(int32_t timeout_us, void *stream);
+
 /* Human-readable name of a status. */
 const char *gemm_status_string(gemm_status s);
 

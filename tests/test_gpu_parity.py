@@ -256,3 +256,15 @@ def test_kernel_resources_match_planner(bm, bn):
         regs, occ = B.gemm_tc_kernel_info(bm, bn, dtype)
         assert 0 < regs <= assumed
         assert occ >= want_bpc
+
+
+def test_bounded_wait_gives_up_and_reports():
+    # a wait on a barrier nothing completes must end with an error status the
+    # host reads, and leave the context usable
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+    B.gemm_selftest_wait_timeout(20000)
+    assert B.gemm_device_error() == (B.GEMM_ERR_TIMEOUT, 5)
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+    A = workloads.random_i8((256, 300), 31)
+    Bt = workloads.random_i8((200, 300), 32)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
