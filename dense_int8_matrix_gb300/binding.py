@@ -32,12 +32,14 @@ GEMM_KERNEL_SKINNY = 2
 GEMM_KERNEL_KINDS = 3
 GEMM_PLAN_VERSION = 1
 GEMM_I8_MAX_K = 131071
+GEMM_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 # every function the header declares
 EXPORTED = (
     "gemm_i8_plan", "gemm_bf16_plan", "gemm_plan_for_sms", "gemm_i8_run", "gemm_bf16_run",
     "gemm_i8_run_host", "gemm_bf16_run_host", "gemm_device_error", "gemm_trace_begin",
     "gemm_trace_collect", "gemm_tc_kernel_info", "gemm_selftest_wait_timeout", "gemm_status_string",
+    "gemm_i8_run_noalloc",
 )
 
 
@@ -104,6 +106,7 @@ def load():
         "gemm_trace_collect": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)],
         "gemm_tc_kernel_info": [i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "gemm_selftest_wait_timeout": [i32, vp],
+        "gemm_i8_run_noalloc": [P, vp, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -192,6 +195,16 @@ def gemm_bf16_run(plan: gemm_plan, A, Bt, C, stream=None) -> None:
                               _addr(Bt, torch.bfloat16, (n, k)), _addr(C, torch.float32, (m, n)),
                               _stream(stream))
     _check(st, "gemm_bf16_run")
+
+
+def gemm_i8_run_noalloc(plan: gemm_plan, A, Bt, C, stream=None) -> None:
+    """gemm_i8_run without device allocation (fixed 64 MiB static scratch)."""
+    import torch
+    m, k, n = plan.m, plan.k, plan.n
+    st = load().gemm_i8_run_noalloc(ctypes.byref(plan), _addr(A, torch.int8, (m, k)),
+                                    _addr(Bt, torch.int8, (n, k)), _addr(C, torch.int32, (m, n)),
+                                    _stream(stream))
+    _check(st, "gemm_i8_run_noalloc")
 
 
 def gemm_i8_run_host(plan: gemm_plan, A, Bt, C, stream=None) -> None:

@@ -1,0 +1,144 @@
+// gemm_i8_run_noalloc: the int8 GEMM without any device-memory allocation.
+//
+// Who needs it: callers that are not allowed to allocate device memory
+// themselves or through a library they call — runtimes that plan every byte
+// of device memory up front and forbid libraries to grab more, and
+// latency-critical loops where an allocation could block, synchronise the
+// device or fail part-way through a run.  gemm_i8_run takes its f16 operand
+// copies from a stream-ordered pool; this entry point uses instead a fixed
+// scratch array that lives in the library's own device image.
+//
+// The scratch is a file-scope static __device__ array of kNoAllocScratchBytes
+// (64 MiB).  Every GPU that loads the library holds it until the process
+// exits, whether or not this entry point is ever called.  In host code the
+// array's name is only a host-side stand-in, not a device address, so the
+// first call on each device (with that device current) looks its device
+// address up with cudaGetSymbolAddress and caches it; that first call should
+// come before any stream capture.
+//
+// All calls share the one array and it keeps the last call's contents.  The
+// staging kernel overwrites every element the GEMM reads (the pad columns of
+// each row are never read), and the variant's time-out word is cleared at the
+// start of each call.  Calls whose work overlaps on the GPU (on different
+// streams, or on different host threads without ordering) race on the array
+// and give wrong results: order them.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/dense_int8_matrix.h"
+#include "internal.h"
+
+namespace gemm {
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // GEMM_NOALLOC_SCRATCH_BYTES
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// Time-out word of this variant's kernels (the allocating entry points use
+// their own word, read by gemm_device_error).
+static __device__ int g_noalloc_err;
+
+constexpr int kMaxDevices = 64;
+
+struct NoAllocDevice {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch
+    int* err = nullptr;                 // device address of g_noalloc_err
+};
+
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+
+// Once per device, with the device current: attributes and the device
+// addresses of the static arrays.  No allocation.
+gemm_status noalloc_device(NoAllocDevice** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
+            d.scratch = static_cast<unsigned char*>(p);
+            p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_err) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
+            d.err = static_cast<int*>(p);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+
+}  // namespace
+
+}  // namespace gemm
+
+extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, const int8_t* Bt, int32_t* C,
+                                           void* stream_ptr) {
+    using namespace gemm;
+    if (!p || p->version != GEMM_PLAN_VERSION || p->dtype != GEMM_DTYPE_I8) return GEMM_ERR_INVALID_ARG;
+    if (p->m < 1 || p->k < 1 || p->n < 1) return GEMM_ERR_INVALID_ARG;
+    if (!A || !Bt || !C) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bt)) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(C) % 4 != 0)
+        return GEMM_ERR_MISALIGNED;
+    const bool skinny = p->path == GEMM_PATH_SKINNY;
+    if (skinny) {
+        if (p->m > 64) return GEMM_ERR_INVALID_ARG;
+    } else {
+        if (p->path != GEMM_PATH_TENSOR || (p->bm != 64 && p->bm != 128) ||
+            (p->bn != 32 && p->bn != 64 && p->bn != 128 && p->bn != 256) || p->grid < 1 || p->k_pitch < p->k ||
+            (p->k_pitch % 8) != 0 || p->chunk_k < kTcBK || (p->chunk_k % kTcBK) != 0 || p->chunk_k > kI8ChunkK)
+            return GEMM_ERR_INVALID_ARG;
+        // the f16 copies of A and Bt must fit the static scratch array
+        const int64_t need = round256(p->m * p->k_pitch * 2) + round256(p->n * p->k_pitch * 2);
+        if (need > static_cast<int64_t>(kNoAllocScratchBytes)) return GEMM_ERR_INVALID_ARG;
+    }
+    NoAllocDevice* d = nullptr;
+    gemm_status st = noalloc_device(&d);
+    if (st != GEMM_OK) return st;
+    if (!d->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    if (skinny)
+        return launch_skinny_i8(A, Bt, C, p->m, p->n, p->k, d->num_sms, stream) == cudaSuccess ? GEMM_OK
+                                                                                               : GEMM_ERR_CUDA;
+
+    if (!tensor_map_encoder_available()) return GEMM_ERR_CUDA;
+    if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    uint16_t* Ah = reinterpret_cast<uint16_t*>(d->scratch);
+    uint16_t* Bh = reinterpret_cast<uint16_t*>(d->scratch + round256(p->m * p->k_pitch * 2));
+    if (launch_stage_i8(A, Bt, Ah, Bh, p->m, p->n, p->k, p->k_pitch, d->num_sms, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    TcLaunch L;
+    L.A16 = Ah;
+    L.B16 = Bh;
+    L.C = C;
+    L.err = d->err;
+    L.m = p->m;
+    L.n = p->n;
+    L.k = p->k;
+    L.k_pitch = p->k_pitch;
+    L.bm = p->bm;
+    L.bn = p->bn;
+    L.grid = p->grid;
+    L.chunk_kb = p->chunk_k / kTcBK;
+    L.int_out = true;
+    return launch_tc(L, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}

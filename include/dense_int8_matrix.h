@@ -134,6 +134,39 @@ gemm_status gemm_bf16_run(const gemm_plan *plan, const uint16_t *A, const uint16
                           void *stream);
 
 /*
+ * gemm_i8_run without any device-memory allocation.  The pages have no
+ * counterpart to this entry point.
+ *
+ * For callers that may not allocate device memory, directly or through a
+ * library: runtimes that plan all device memory up front and forbid libraries
+ * to take more, and latency-critical loops where an allocation could block,
+ * synchronise the device or fail mid-run.  The f16 operand copies that
+ * gemm_i8_run takes from a memory pool go instead into one fixed scratch
+ * array of GEMM_NOALLOC_SCRATCH_BYTES (64 MiB) in the library's device image,
+ * which every GPU that loads the library holds until the process exits.  The
+ * call makes no cudaMalloc, cudaFree or other allocating call.
+ *
+ * Same arguments, rules and result as gemm_i8_run (the skinny path needs no
+ * scratch and runs unchanged).  Extra rules:
+ *   - the tensor-core path needs round256(m*k_pitch*2) + round256(n*k_pitch*2)
+ *     bytes of scratch; larger problems return GEMM_ERR_INVALID_ARG and
+ *     launch nothing;
+ *   - the first call on each device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture;
+ *   - every call shares the one array and it keeps the last call's contents
+ *     (each call overwrites what it reads and clears its own time-out word),
+ *     so calls whose work overlaps on the GPU race and give wrong results:
+ *     order them on one stream or with events;
+ *   - a kernel wait that runs past its limit ends this variant's kernels
+ *     early (C incomplete) and is recorded in the variant's own device word,
+ *     which gemm_device_error does not read.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (64ll << 20)
+gemm_status gemm_i8_run_noalloc(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
+                                void *stream);
+
+/*
  * End-to-end forms: A, Bt and C are HOST pointers (pinned or pageable).  The
  * call takes device buffers from the library's pool, copies A and Bt to the
  * device, runs the plan, copies C back and waits for `stream` to finish, so

@@ -1,0 +1,67 @@
+"""The allocation-free int8 entry point, gemm_i8_run_noalloc, against
+gemm_i8_run.
+
+Some callers cannot let a library allocate device memory (memory-planned
+runtimes, latency-critical loops); for them gemm_i8_run_noalloc stages its
+f16 operand copies in a fixed static device array instead of a memory pool.
+Its results must equal gemm_i8_run's bit for bit, on consecutive calls that
+reuse the shared array.  This file is collected last on purpose."""
+
+import ctypes
+
+import pytest
+import torch
+
+from dense_int8_matrix_gb300 import binding as B
+from dense_int8_matrix_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_int8_matrix_gb300 import build
+    build.build()
+    B.load()
+
+
+def _both(m, k, n, seed):
+    A = workloads.random_i8((m, k), seed).cuda()
+    Bt = workloads.random_i8((n, k), seed + 1).cuda()
+    plan = B.gemm_i8_plan(m, k, n)
+    ref = torch.empty((m, n), dtype=torch.int32, device="cuda")
+    B.gemm_i8_run(plan, A, Bt, ref)
+    out = torch.full((m, n), -7, dtype=torch.int32, device="cuda")
+    lib = B.load()
+    st = lib.gemm_i8_run_noalloc(ctypes.byref(plan), A.data_ptr(), Bt.data_ptr(), out.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert st == B.GEMM_OK, B.gemm_status_string(st)
+    torch.cuda.synchronize()
+    return out, ref
+
+
+def test_noalloc_matches_allocating_entry_point_twice():
+    # two calls in a row through the C ABI; the second reuses the static
+    # scratch the first one filled (different shapes, so stale contents
+    # would show)
+    for m, k, n, seed in [(1000, 2100, 3000, 11), (700, 777, 520, 12)]:
+        out, ref = _both(m, k, n, seed)
+        assert torch.equal(out, ref)
+
+
+def test_noalloc_largest_problem_and_rejection():
+    # 4096^3 needs exactly the 64 MiB of scratch
+    out, ref = _both(4096, 4096, 4096, 13)
+    assert torch.equal(out, ref)
+    lib = B.load()
+    plan = B.gemm_i8_plan(4096, 4104, 4096)        # needs more than 64 MiB
+    buf = torch.empty(16, dtype=torch.int8, device="cuda")
+    st = lib.gemm_i8_run_noalloc(ctypes.byref(plan), buf.data_ptr(), buf.data_ptr(), buf.data_ptr(), None)
+    assert st == B.GEMM_ERR_INVALID_ARG
+
+
+def test_noalloc_skinny_plan():
+    out, ref = _both(16, 4096, 1000, 14)
+    assert torch.equal(out, ref)
