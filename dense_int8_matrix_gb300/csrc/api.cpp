@@ -109,6 +109,8 @@ gemm_status check_plan(const gemm_plan* p, int32_t dtype) {
         (p->chunk_k % kTcBK) != 0)
         return GEMM_ERR_INVALID_ARG;
     if (dtype == GEMM_DTYPE_I8 && p->chunk_k > kI8ChunkK) return GEMM_ERR_INVALID_ARG;
+    // bf16 problems accumulate the whole K in one TMEM chunk
+    if (dtype == GEMM_DTYPE_BF16 && p->chunk_k < p->k) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }
 

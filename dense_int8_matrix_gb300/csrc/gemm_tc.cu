@@ -29,6 +29,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -48,15 +49,18 @@ struct TcCfg {
     static constexpr int HALF = BN / 2;                 // columns per epilogue thread
     static constexpr int SLICE = HALF >= 32 ? 32 : 16;  // columns per tcgen05.ld
     static constexpr int NSLICE = HALF / SLICE;
+    static constexpr bool TMA_STORE = tc_tma_store_tile(BM, BN);
+    static constexpr int EPI_BYTES = TMA_STORE ? kTcEpilogueWarps * kTcEpiStageBytes : 0;
     static constexpr size_t SMEM = tc_smem_bytes(BM, BN);
     static_assert(BM == 64 || BM == 128, "BM");
     static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN");
-    static_assert(kTcStages * STAGE_BYTES + 1024 + 8 * (2 * kTcStages + 5) + 8 <= SMEM, "smem layout");
+    static_assert(kTcStages * STAGE_BYTES + EPI_BYTES + 1024 + 8 * (2 * kTcStages + 5) + 8 <= SMEM, "smem layout");
 };
 
 struct TcParams {
     void* C;
     int* err;
+    int c_tma;      // 1: write C with TMA stores (wide tiles, n % 4 == 0, C 16-byte aligned)
     int64_t m, n;
     int num_kb;     // ceil(k / 64)
     int chunk_kb;   // K steps per accumulator chunk
@@ -75,10 +79,10 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, i
     tn = local / rows_in_band;
 }
 
-template <int BM, int BN, bool INT_OUT>
+template <int BM, int BN, bool INT_OUT, bool C_TMA>
 __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     using Cfg = TcCfg<BM, BN>;
     extern __shared__ uint8_t smem_raw[];
 
@@ -86,7 +90,8 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sA = base;
     const uint32_t sB = base + kTcStages * Cfg::A_BYTES;
-    uint8_t* ctrl = smem_raw + (base - raw) + kTcStages * Cfg::STAGE_BYTES;
+    const uint32_t sEpi = base + kTcStages * Cfg::STAGE_BYTES;   // 8 x 4 KiB, 1024-aligned
+    uint8_t* ctrl = smem_raw + (base - raw) + kTcStages * Cfg::STAGE_BYTES + Cfg::EPI_BYTES;
     const uint32_t bar0 = smem_u32(ctrl);
     // barrier slots: full[S], empty[S], acc_full[2], acc_empty[2], done
     const uint32_t full_bar0 = bar0;
@@ -127,6 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            if (C_TMA) tma_prefetch_desc(&tmC);
             const uint64_t pol = policy_evict_normal();
             uint32_t issued = 0;
             bool ok = true;
@@ -202,20 +208,25 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
         const int e = warp - 4;
         const int q = warp & 3;     // TMEM lane quarter this warp can access
         const int h = e >> 2;       // which half of the BN columns
-        using Acc = typename std::conditional<INT_OUT, int32_t, float>::type;
         uint32_t acc_iter = 0;
         bool ok = true;
         const bool row_valid = (BM == 128) || (lane < 16);
         const int row_in_tile = (BM == 128) ? (q * 32 + lane) : (q * 16 + lane);
+        const bool c_vec = ((p.n & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
             int tm, tn;
             tile_coords(t, p, tm, tn);
-            Acc acc[Cfg::HALF];
+            const int64_t row = static_cast<int64_t>(tm) * BM + row_in_tile;
+            const int64_t col0 = static_cast<int64_t>(tn) * BN + h * Cfg::HALF;
+            // int8 problems: exact int32 running sums over the K chunks; bf16
+            // problems have a single chunk and need none
+            int32_t acc[INT_OUT ? Cfg::HALF : 1];
 #pragma unroll
-            for (int j = 0; j < Cfg::HALF; ++j) acc[j] = Acc(0);
+            for (int j = 0; j < (INT_OUT ? Cfg::HALF : 1); ++j) acc[j] = 0;
             for (int c0 = 0; c0 < p.num_kb; c0 += p.chunk_kb) {
                 const uint32_t buf = acc_iter & 1u;
                 const uint32_t aph = (acc_iter >> 1) & 1u;
+                const bool last = c0 + p.chunk_kb >= p.num_kb;
                 // lane 0 polls; the warp then reconverges before the
                 // warp-collective tcgen05.ld
                 int got = 1;
@@ -230,54 +241,84 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                 const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * Cfg::HALF;
 #pragma unroll
                 for (int sl = 0; sl < Cfg::NSLICE; ++sl) {
-                    uint32_t r[Cfg::SLICE];
-                    if constexpr (Cfg::SLICE == 32)
-                        tmem_ld_32x32b_x32(tcol + sl * 32, r);
-                    else
-                        tmem_ld_32x32b_x16(tcol + sl * 16, r);
-                    tmem_wait_ld();
+                    uint32_t r[INT_OUT ? 1 : Cfg::SLICE];
+                    if constexpr (INT_OUT) {
+                        // 16 columns at a time keeps the registers live beside the
+                        // running sums low
 #pragma unroll
-                    for (int j = 0; j < Cfg::SLICE; ++j) {
-                        const float v = __uint_as_float(r[j]);
-                        if constexpr (INT_OUT)
-                            acc[sl * Cfg::SLICE + j] += __float2int_rn(v);   // exact: |v| <= 2^24
+                        for (int half = 0; half < Cfg::SLICE / 16; ++half) {
+                            uint32_t v[16];
+                            tmem_ld_32x32b_x16(tcol + sl * Cfg::SLICE + half * 16, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                // exact: an fp32 chunk sum is an integer of magnitude <= 2^24
+                                acc[sl * Cfg::SLICE + half * 16 + j] += __float2int_rn(__uint_as_float(v[j]));
+                            }
+                        }
+                    } else {
+                        if constexpr (Cfg::SLICE == 32)
+                            tmem_ld_32x32b_x32(tcol + sl * 32, r);
                         else
-                            acc[sl * Cfg::SLICE + j] += v;
+                            tmem_ld_32x32b_x16(tcol + sl * 16, r);
+                        tmem_wait_ld();
                     }
+                    if (!last) continue;
+                    // this slice's final 32-bit results: the int32 sums, or the
+                    // fp32 values as loaded
+#define GEMM_TC_OUT(j) (INT_OUT ? static_cast<uint32_t>(acc[(INT_OUT ? sl * Cfg::SLICE : 0) + (j)]) : r[INT_OUT ? 0 : (j)])
+                    const int64_t cs = col0 + sl * Cfg::SLICE;
+                    if constexpr (C_TMA) {
+                        // Coalesced write-back (the shared-memory staged epilogue of
+                        // "先导杯比赛回顾", section "Epilogue 写回优化"): each lane writes
+                        // its row of the 32-column slice (128 bytes) into the warp's
+                        // 128B-swizzled 4 KiB buffer, then one TMA store moves the
+                        // 32 x 32 box to C; rows / columns outside C are clipped.
+                        static_assert(!C_TMA || Cfg::SLICE == 32, "TMA store slices are 32 columns");
+                        const uint32_t stg = sEpi + e * kTcEpiStageBytes;
+                        const uint32_t row_base = stg + lane * 128;
+                        if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            st_shared_v4(row_base + ((c ^ (lane & 7)) << 4), GEMM_TC_OUT(4 * c), GEMM_TC_OUT(4 * c + 1),
+                                         GEMM_TC_OUT(4 * c + 2), GEMM_TC_OUT(4 * c + 3));
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, stg, static_cast<int32_t>(cs),
+                                         static_cast<int32_t>(static_cast<int64_t>(tm) * BM + q * 32));
+                            bulk_commit();
+                        }
+                    } else {
+                        if (row_valid && row < p.m) {
+                            uint32_t* out = static_cast<uint32_t*>(p.C) + row * p.n + cs;
+                            if (c_vec && cs + Cfg::SLICE <= p.n) {
+#pragma unroll
+                                for (int j = 0; j < Cfg::SLICE; j += 4)
+                                    *reinterpret_cast<uint4*>(out + j) =
+                                        make_uint4(GEMM_TC_OUT(j), GEMM_TC_OUT(j + 1), GEMM_TC_OUT(j + 2), GEMM_TC_OUT(j + 3));
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < Cfg::SLICE; ++j)
+                                    if (cs + j < p.n) out[j] = GEMM_TC_OUT(j);
+                            }
+                        }
+                    }
+#undef GEMM_TC_OUT
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce_bar0 + 8u * buf);
                 ++acc_iter;
             }
-            if (!ok) break;
-            const int64_t row = static_cast<int64_t>(tm) * BM + row_in_tile;
-            const int64_t col0 = static_cast<int64_t>(tn) * BN + h * Cfg::HALF;
-            if (row_valid && row < p.m) {
-                Acc* out = static_cast<Acc*>(p.C) + row * p.n + col0;
-                const bool vec = ((p.n & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
-                                 (col0 + Cfg::HALF <= p.n);
-                if (vec) {
-#pragma unroll
-                    for (int j = 0; j < Cfg::HALF; j += 4) {
-                        int4 v;
-                        if constexpr (INT_OUT) {
-                            v = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                        } else {
-                            v = make_int4(__float_as_int(acc[j]), __float_as_int(acc[j + 1]),
-                                          __float_as_int(acc[j + 2]), __float_as_int(acc[j + 3]));
-                        }
-                        *reinterpret_cast<int4*>(out + j) = v;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < Cfg::HALF; ++j)
-                        if (col0 + j < p.n) out[j] = acc[j];
-                }
-            }
         }
     }
 
+    if constexpr (C_TMA) {
+        // every TMA store of C must complete before the CTA exits
+        if (warp >= 4 && lane == 0) bulk_wait_all();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -330,18 +371,38 @@ cudaError_t configure_kernel(const void* kern, size_t smem) {
                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
 }
 
+// Tensor map of C (m x n, 4-byte elements) for TMA stores: box 32 x 32,
+// 128-byte swizzle.  Needs a 16-byte row pitch and base.
+bool encode_c_map(CUtensorMap* map, void* ptr, int64_t m, int64_t n) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(n) * 4u};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, ptr, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int BM, int BN, bool INT_OUT>
 cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     using Cfg = TcCfg<BM, BN>;
-    auto kern = gemm_tc_kernel<BM, BN, INT_OUT>;
-    cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kern), Cfg::SMEM);
-    if (e != cudaSuccess) return e;
     CUtensorMap mA, mB;
     if (!encode_operand_map(&mA, a.A16, a.m, a.k, a.k_pitch, BM)) return cudaErrorInvalidValue;
     if (!encode_operand_map(&mB, a.B16, a.n, a.k, a.k_pitch, BN)) return cudaErrorInvalidValue;
+    CUtensorMap mC;
+    std::memset(&mC, 0, sizeof(mC));
+    int c_tma = 0;
+    if (Cfg::TMA_STORE && (a.n % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0) {
+        if (!encode_c_map(&mC, a.C, a.m, a.n)) return cudaErrorInvalidValue;
+        c_tma = 1;
+    }
     TcParams p;
     p.C = a.C;
     p.err = a.err;
+    p.c_tma = c_tma;
     p.m = a.m;
     p.n = a.n;
     p.num_kb = static_cast<int>((a.k + kTcBK - 1) / kTcBK);
@@ -349,7 +410,10 @@ cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     p.tiles_m = static_cast<int>((a.m + BM - 1) / BM);
     p.tiles_n = static_cast<int>((a.n + BN - 1) / BN);
     p.tiles = p.tiles_m * p.tiles_n;
-    kern<<<a.grid, kTcThreads, Cfg::SMEM, stream>>>(mA, mB, p);
+    auto kern = c_tma ? gemm_tc_kernel<BM, BN, INT_OUT, Cfg::TMA_STORE> : gemm_tc_kernel<BM, BN, INT_OUT, false>;
+    cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kern), Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<a.grid, kTcThreads, Cfg::SMEM, stream>>>(mA, mB, mC, p);
     return cudaGetLastError();
 }
 
@@ -371,7 +435,7 @@ cudaError_t dispatch(const TcLaunch& a, cudaStream_t stream) {
 
 template <int BM, int BN, bool INT_OUT>
 const void* kernel_ptr() {
-    return reinterpret_cast<const void*>(gemm_tc_kernel<BM, BN, INT_OUT>);
+    return reinterpret_cast<const void*>(gemm_tc_kernel<BM, BN, INT_OUT, TcCfg<BM, BN>::TMA_STORE>);
 }
 
 const void* find_kernel(int bm, int bn, bool int_out) {

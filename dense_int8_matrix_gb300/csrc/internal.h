@@ -31,10 +31,17 @@ constexpr int tc_tmem_cols(int bn) {
     return cols;
 }
 
+// Wide tiles (BM = 128, BN >= 128) write C through shared memory and TMA
+// stores: each epilogue warp stages 32 rows x 32 columns of 4-byte values
+// (4 KiB, 128-byte swizzle) at a time.
+constexpr bool tc_tma_store_tile(int bm, int bn) { return bm == 128 && bn >= 128; }
+constexpr int kTcEpiStageBytes = 32 * 32 * 4;
+
 constexpr size_t tc_smem_bytes(int bm, int bn) {
-    // operand ring + 1 KiB to align it to the 1024-byte swizzle atom +
-    // 1 KiB for barriers and flags
-    return static_cast<size_t>(kTcStages) * (bm + bn) * kTcRowBytes + 1024 + 1024;
+    // operand ring + epilogue staging + 1 KiB to align to the 1024-byte
+    // swizzle atom + 1 KiB for barriers and flags
+    return static_cast<size_t>(kTcStages) * (bm + bn) * kTcRowBytes +
+           (tc_tma_store_tile(bm, bn) ? static_cast<size_t>(kTcEpilogueWarps) * kTcEpiStageBytes : 0) + 1024 + 1024;
 }
 
 // Registers per thread the kernel is compiled for (launch bounds): wide

@@ -39,30 +39,44 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return v;
 }
 
-// Contiguous rows (k == k_pitch, k % 16 == 0): 16 int8 -> 16 f16 per item.
+__device__ __forceinline__ void convert16(const uint4 v, uint4* d) {
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+    uint4 lo, hi;
+    lo.x = i8x2_to_f16x2(w[0], 0x4140u);
+    lo.y = i8x2_to_f16x2(w[0], 0x4342u);
+    lo.z = i8x2_to_f16x2(w[1], 0x4140u);
+    lo.w = i8x2_to_f16x2(w[1], 0x4342u);
+    hi.x = i8x2_to_f16x2(w[2], 0x4140u);
+    hi.y = i8x2_to_f16x2(w[2], 0x4342u);
+    hi.z = i8x2_to_f16x2(w[3], 0x4140u);
+    hi.w = i8x2_to_f16x2(w[3], 0x4342u);
+    d[0] = lo;
+    d[1] = hi;
+}
+
+constexpr int kStageUnroll = 4;
+
+// Contiguous rows (k == k_pitch, k % 16 == 0): 16 int8 -> 16 f16 per item;
+// each thread keeps kStageUnroll loads in flight.
 __global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restrict__ srcA,
                                                             const uint4* __restrict__ srcB, uint4* __restrict__ dstA,
                                                             uint4* __restrict__ dstB, int64_t itemsA,
                                                             int64_t itemsB) {
     const int64_t total = itemsA + itemsB;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const bool isA = i < itemsA;
-        const int64_t j = isA ? i : i - itemsA;
-        const uint4 v = ld_stream((isA ? srcA : srcB) + j);
-        const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-        uint4 lo, hi;
-        lo.x = i8x2_to_f16x2(w[0], 0x4140u);
-        lo.y = i8x2_to_f16x2(w[0], 0x4342u);
-        lo.z = i8x2_to_f16x2(w[1], 0x4140u);
-        lo.w = i8x2_to_f16x2(w[1], 0x4342u);
-        hi.x = i8x2_to_f16x2(w[2], 0x4140u);
-        hi.y = i8x2_to_f16x2(w[2], 0x4342u);
-        hi.z = i8x2_to_f16x2(w[3], 0x4140u);
-        hi.w = i8x2_to_f16x2(w[3], 0x4342u);
-        uint4* d = (isA ? dstA : dstB) + 2 * j;
-        d[0] = lo;
-        d[1] = hi;
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+         i0 += stride * kStageUnroll) {
+        uint4 v[kStageUnroll];
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < total) v[u] = ld_stream(i < itemsA ? srcA + i : srcB + (i - itemsA));
+        }
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < total) convert16(v[u], i < itemsA ? dstA + 2 * i : dstB + 2 * (i - itemsA));
+        }
     }
 }
 

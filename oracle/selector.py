@@ -61,8 +61,10 @@ def regs_per_thread(bn: int) -> int:
 
 def smem_per_cta(bm: int, bn: int) -> int:
     # operand ring + 1 KiB for aligning the ring to the 1024-byte swizzle
-    # atom + 1 KiB for barriers and bookkeeping
-    return STAGES * (bm + bn) * BK_ELEMS * ESIZE + 1024 + 1024
+    # atom + 1 KiB for barriers and bookkeeping; wide tiles (BM = 128,
+    # BN >= 128) also stage C for TMA stores in 8 buffers of 4 KiB
+    epilogue = 8 * 4096 if (bm == 128 and bn >= 128) else 0
+    return STAGES * (bm + bn) * BK_ELEMS * ESIZE + epilogue + 1024 + 1024
 
 
 def tmem_cols(bn: int) -> int:

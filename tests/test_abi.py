@@ -127,6 +127,9 @@ def test_run_argument_errors_before_any_launch(lib):
     bad = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 256, 256, 256, 148)
     bad.chunk_k = 2048   # would break the exactness bound of the int8 path
     assert lib.gemm_i8_run(ctypes.byref(bad), 4096, 4096, 4096, s) == B.GEMM_ERR_INVALID_ARG
+    badb = B.gemm_plan_for_sms(B.GEMM_DTYPE_BF16, 256, 1000, 256, 148)
+    badb.chunk_k = 512   # bf16 accumulates the whole K in one chunk
+    assert lib.gemm_bf16_run(ctypes.byref(badb), 4096, 4096, 4096, s) == B.GEMM_ERR_INVALID_ARG
     bad = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 256, 256, 256, 148)
     bad.k_pitch = 100
     assert lib.gemm_i8_run(ctypes.byref(bad), 4096, 4096, 4096, s) == B.GEMM_ERR_INVALID_ARG

@@ -43,7 +43,8 @@ def test_selector_ratio_closed_form():
     for b in (64, 128):
         assert selector.ratio(b, b) == b / 2
     # the traffic of a (BM, BN) tile per K step is (BM + BN) * BK * 2 bytes
-    assert selector.smem_per_cta(128, 256) == 4 * 384 * 128 + 2048
+    assert selector.smem_per_cta(128, 256) == 4 * 384 * 128 + 8 * 4096 + 2048
+    assert selector.smem_per_cta(64, 256) == 4 * 320 * 128 + 2048
 
 
 def test_every_candidate_fits():
