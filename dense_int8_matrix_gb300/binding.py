@@ -30,7 +30,7 @@ GEMM_KERNEL_STAGE = 0
 GEMM_KERNEL_TC = 1
 GEMM_KERNEL_SKINNY = 2
 GEMM_KERNEL_KINDS = 3
-GEMM_PLAN_VERSION = 1
+GEMM_PLAN_VERSION = 2
 GEMM_I8_MAX_K = 131071
 GEMM_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -51,9 +51,10 @@ class gemm_plan(ctypes.Structure):
         ("bm", ctypes.c_int32), ("bn", ctypes.c_int32), ("bk", ctypes.c_int32),
         ("stages", ctypes.c_int32), ("tiles", ctypes.c_int32), ("bpc", ctypes.c_int32),
         ("grid", ctypes.c_int32), ("waves", ctypes.c_int32), ("k_pitch", ctypes.c_int32),
-        ("chunk_k", ctypes.c_int32), ("fallback", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("chunk_k", ctypes.c_int32), ("fallback", ctypes.c_int32), ("split_k", ctypes.c_int32),
         ("ratio", ctypes.c_double), ("workspace_bytes", ctypes.c_int64),
-        ("reserved", ctypes.c_int64 * 4),
+        ("split_from", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("reserved", ctypes.c_int64 * 3),
     ]
 
     def as_dict(self):

@@ -131,22 +131,45 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
 
     const bool is_i8 = p->dtype == GEMM_DTYPE_I8;
     const bool need_stage = is_i8 || (p->k_pitch != p->k);
+    const int chunk_kb = p->chunk_k / kTcBK;
+
+    // Tail split, recomputed for the tile and grid actually launched; only
+    // when every CTA of the grid can be resident at once (slices wait for
+    // slice 0 of their tile, which must be running).
+    const int64_t tiles = ((p->m + p->bm - 1) / p->bm) * ((p->n + p->bn - 1) / p->bn);
+    int64_t split_from = tiles;
+    int split = 1;
+    {
+        const int64_t num_kb = (p->k + kTcBK - 1) / kTcBK;
+        const int64_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
+        const int64_t capacity = static_cast<int64_t>(ds->num_sms) * tc_blocks_per_sm(p->bm, p->bn);
+        if (p->grid <= capacity) split = tc_tail_split(tiles, p->grid, nchunks, is_i8, &split_from);
+        if (split > 1 && tiles - split_from > kTcSplitFlagTiles) split = 1;
+        if (split == 1) split_from = tiles;
+    }
+    // one flag per (split tile, epilogue warp), zeroed by the staging kernel
+    const int64_t flag_count = (tiles - split_from) * kTcEpilogueWarps;
+
     void* ws = nullptr;
     const void* A16 = A;
     const void* B16 = Bt;
+    int* flags = nullptr;
     if (need_stage) {
         const int64_t a_bytes = ((p->m * p->k_pitch * 2 + 255) / 256) * 256;
         const int64_t b_bytes = ((p->n * p->k_pitch * 2 + 255) / 256) * 256;
-        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes), ds->pool, stream) != cudaSuccess)
+        const int64_t f_bytes = ((flag_count * 4 + 255) / 256) * 256;
+        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes + f_bytes), ds->pool, stream) !=
+            cudaSuccess)
             return GEMM_ERR_CUDA;
         uint16_t* Ah = static_cast<uint16_t*>(ws);
         uint16_t* Bh = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + a_bytes);
+        if (flag_count > 0) flags = reinterpret_cast<int*>(static_cast<char*>(ws) + a_bytes + b_bytes);
         cudaError_t e;
         {
             TraceScope t(GEMM_KERNEL_STAGE, stream);
             if (is_i8)
                 e = launch_stage_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), Ah, Bh, p->m, p->n,
-                                    p->k, p->k_pitch, ds->num_sms, stream);
+                                    p->k, p->k_pitch, flags, flag_count, ds->num_sms, stream);
             else
                 e = launch_stage_b16(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(Bt), Ah, Bh, p->m,
                                      p->n, p->k, p->k_pitch, ds->num_sms, stream);
@@ -171,8 +194,12 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     L.bm = p->bm;
     L.bn = p->bn;
     L.grid = p->grid;
-    L.chunk_kb = p->chunk_k / kTcBK;
+    L.chunk_kb = chunk_kb;
     L.int_out = is_i8;
+    L.split_k = flags ? split : 1;
+    L.split_from = flags ? split_from : tiles;
+    L.split_flags = flags;
+    L.epoch = 1;
     cudaError_t e;
     {
         TraceScope t(GEMM_KERNEL_TC, stream);

@@ -65,6 +65,11 @@ struct TcParams {
     int num_kb;     // ceil(k / 64)
     int chunk_kb;   // K steps per accumulator chunk
     int tiles_m, tiles_n, tiles;
+    int units;      // split_from + (tiles - split_from) * split_k
+    int split_from; // tiles [split_from, tiles) run as split_k K slices each
+    int split_k;
+    uint32_t* split_flags;
+    uint32_t epoch;
 };
 
 constexpr int kBandM = 8;
@@ -77,6 +82,67 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, i
     const int local = t - band * per_band;
     tm = first_m + local % rows_in_band;
     tn = local / rows_in_band;
+}
+
+// A unit of work: one tile over the K steps [kb_lo, kb_hi).  Units below
+// split_from are whole tiles; above it, the slices of a split tile are
+// consecutive units (so they run in the same round on different CTAs), each
+// a run of whole accumulator chunks.
+struct Unit {
+    int tm, tn, kb_lo, kb_hi;
+    int split_tile;   // index among the split tiles, -1 if the tile is whole
+    int slice;
+};
+
+__device__ __forceinline__ Unit unit_at(int u, const TcParams& p) {
+    Unit x;
+    int t;
+    if (u < p.split_from) {
+        t = u;
+        x.kb_lo = 0;
+        x.kb_hi = p.num_kb;
+        x.split_tile = -1;
+        x.slice = 0;
+    } else {
+        const int v = u - p.split_from;
+        x.split_tile = v / p.split_k;
+        x.slice = v - x.split_tile * p.split_k;
+        t = p.split_from + x.split_tile;
+        const int nch = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
+        x.kb_lo = (x.slice * nch / p.split_k) * p.chunk_kb;
+        x.kb_hi = min(p.num_kb, ((x.slice + 1) * nch / p.split_k) * p.chunk_kb);
+    }
+    tile_coords(t, p, x.tm, x.tn);
+    return x;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* addr, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Wait (bounded) until *flag == epoch; on time-out raise the abort flag and
+// record the error.
+__device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t epoch, volatile uint32_t* abort_flag,
+                                                  int* err) {
+    if (ld_acquire_gpu(flag) == epoch) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < kWaitIterCap; ++it) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) == epoch) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+        }
+    }
+    *abort_flag = 1u;
+    atomicCAS(err, 0, kDevErrTimeoutSplit);
+    return false;
 }
 
 template <int BM, int BN, bool INT_OUT, bool C_TMA>
@@ -136,10 +202,10 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
             const uint64_t pol = policy_evict_normal();
             uint32_t issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
-                int tm, tn;
-                tile_coords(t, p, tm, tn);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                const Unit w = unit_at(u, p);
+                const int tm = w.tm, tn = w.tn;
+                for (int kb = w.kb_lo; kb < w.kb_hi; ++kb) {
                     const uint32_t s = issued % kTcStages;
                     const uint32_t ph = (issued / kTcStages) & 1u;
                     if (!wait_bounded(empty_bar0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) {
@@ -164,8 +230,9 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
             constexpr uint32_t idesc = idesc_f16(INT_OUT ? 0u : 1u, BM, BN);
             uint32_t consumed = 0, acc_iter = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
-                for (int c0 = 0; ok && c0 < p.num_kb; c0 += p.chunk_kb) {
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                const Unit w = unit_at(u, p);
+                for (int c0 = w.kb_lo; ok && c0 < w.kb_hi; c0 += p.chunk_kb) {
                     const uint32_t buf = acc_iter & 1u;
                     const uint32_t aph = (acc_iter >> 1) & 1u;
                     if (!wait_bounded(acce_bar0 + 8u * buf, aph ^ 1u, abort_flag, p.err, kDevErrTimeoutMma)) {
@@ -174,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    const int c1 = min(p.num_kb, c0 + p.chunk_kb);
+                    const int c1 = min(w.kb_hi, c0 + p.chunk_kb);
                     for (int kb = c0; kb < c1; ++kb) {
                         const uint32_t s = consumed % kTcStages;
                         const uint32_t ph = (consumed / kTcStages) & 1u;
@@ -213,9 +280,12 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
         const bool row_valid = (BM == 128) || (lane < 16);
         const int row_in_tile = (BM == 128) ? (q * 32 + lane) : (q * 16 + lane);
         const bool c_vec = ((p.n & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
-        for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
-            int tm, tn;
-            tile_coords(t, p, tm, tn);
+        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            const Unit w = unit_at(u, p);
+            const int tm = w.tm, tn = w.tn;
+            // slices 1.. of a split tile add into C after slice 0 has stored
+            const bool add_into = w.split_tile >= 0 && w.slice > 0;
+            uint32_t* flag = w.split_tile >= 0 ? p.split_flags + w.split_tile * kTcEpilogueWarps + e : nullptr;
             const int64_t row = static_cast<int64_t>(tm) * BM + row_in_tile;
             const int64_t col0 = static_cast<int64_t>(tn) * BN + h * Cfg::HALF;
             // int8 problems: exact int32 running sums over the K chunks; bf16
@@ -223,10 +293,10 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
             int32_t acc[INT_OUT ? Cfg::HALF : 1];
 #pragma unroll
             for (int j = 0; j < (INT_OUT ? Cfg::HALF : 1); ++j) acc[j] = 0;
-            for (int c0 = 0; c0 < p.num_kb; c0 += p.chunk_kb) {
+            for (int c0 = w.kb_lo; c0 < w.kb_hi; c0 += p.chunk_kb) {
                 const uint32_t buf = acc_iter & 1u;
                 const uint32_t aph = (acc_iter >> 1) & 1u;
-                const bool last = c0 + p.chunk_kb >= p.num_kb;
+                const bool last = c0 + p.chunk_kb >= w.kb_hi;
                 // lane 0 polls; the warp then reconverges before the
                 // warp-collective tcgen05.ld
                 int got = 1;
@@ -238,6 +308,16 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                     break;
                 }
                 tc_fence_after();
+                if (last && add_into) {
+                    // this warp's region of C must hold slice 0's values first
+                    if (lane == 0) got = wait_flag_bounded(flag, p.epoch, abort_flag, p.err) ? 1 : 0;
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                }
                 const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * Cfg::HALF;
 #pragma unroll
                 for (int sl = 0; sl < Cfg::NSLICE; ++sl) {
@@ -286,14 +366,21 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&tmC, stg, static_cast<int32_t>(cs),
-                                         static_cast<int32_t>(static_cast<int64_t>(tm) * BM + q * 32));
+                            const int32_t ys = static_cast<int32_t>(static_cast<int64_t>(tm) * BM + q * 32);
+                            if (add_into)
+                                tma_reduce_add_2d(&tmC, stg, static_cast<int32_t>(cs), ys);
+                            else
+                                tma_store_2d(&tmC, stg, static_cast<int32_t>(cs), ys);
                             bulk_commit();
                         }
                     } else {
                         if (row_valid && row < p.m) {
                             uint32_t* out = static_cast<uint32_t*>(p.C) + row * p.n + cs;
-                            if (c_vec && cs + Cfg::SLICE <= p.n) {
+                            if (add_into) {
+#pragma unroll
+                                for (int j = 0; j < Cfg::SLICE; ++j)
+                                    if (cs + j < p.n) atomicAdd(out + j, GEMM_TC_OUT(j));
+                            } else if (c_vec && cs + Cfg::SLICE <= p.n) {
 #pragma unroll
                                 for (int j = 0; j < Cfg::SLICE; j += 4)
                                     *reinterpret_cast<uint4*>(out + j) =
@@ -311,6 +398,18 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce_bar0 + 8u * buf);
                 ++acc_iter;
+                if (last && w.split_tile >= 0 && w.slice == 0) {
+                    // publish: this warp's region of C holds slice 0's values
+                    if constexpr (C_TMA) {
+                        if (lane == 0) bulk_wait_all();
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) {
+                        fence_proxy_async_global();
+                        st_release_gpu(flag, p.epoch);
+                    }
+                }
             }
         }
     }
@@ -410,6 +509,11 @@ cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     p.tiles_m = static_cast<int>((a.m + BM - 1) / BM);
     p.tiles_n = static_cast<int>((a.n + BN - 1) / BN);
     p.tiles = p.tiles_m * p.tiles_n;
+    p.split_k = a.split_k > 1 ? a.split_k : 1;
+    p.split_from = p.split_k > 1 ? static_cast<int>(a.split_from) : p.tiles;
+    p.units = p.split_from + (p.tiles - p.split_from) * p.split_k;
+    p.split_flags = reinterpret_cast<uint32_t*>(a.split_flags);
+    p.epoch = a.epoch;
     auto kern = c_tma ? gemm_tc_kernel<BM, BN, INT_OUT, Cfg::TMA_STORE> : gemm_tc_kernel<BM, BN, INT_OUT, false>;
     cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;

@@ -50,6 +50,31 @@ constexpr size_t tc_smem_bytes(int bm, int bn) {
 constexpr int tc_regs_per_thread(int bn) { return bn >= 128 ? 168 : 80; }
 constexpr int tc_min_blocks(int bn) { return bn >= 128 ? 1 : 2; }
 
+// Tail split of the last, partial wave (int8 only).  With T tiles run by a
+// persistent grid of G co-resident CTAs, R = T / G whole rounds run unsplit;
+// the remaining T - R*G tiles are each split along K into S slices, S as large
+// as fits the grid (S * tail <= G) and at most the number of K chunks (8 at
+// most).  Returns S (1 = no split) and sets *split_from = R * G.
+constexpr int kTcMaxSplit = 8;
+inline int tc_tail_split(int64_t tiles, int64_t grid, int64_t nchunks, bool int_out, int64_t* split_from) {
+    *split_from = tiles;
+    if (!int_out || grid < 2 || tiles <= grid || nchunks < 2) return 1;
+    const int64_t full = (tiles / grid) * grid;
+    const int64_t tail = tiles - full;
+    if (tail == 0) return 1;
+    int64_t s = grid / tail;
+    if (s > nchunks) s = nchunks;
+    if (s > kTcMaxSplit) s = kTcMaxSplit;
+    if (s < 2) return 1;
+    *split_from = full;
+    return static_cast<int>(s);
+}
+
+// Flags of the tail split: one int per (split tile, epilogue warp), zeroed
+// before the launch and set to the launch's epoch once slice 0 of that tile
+// has stored that warp's region of C.
+constexpr int kTcSplitFlagTiles = 4096;
+
 struct TcLaunch {
     const void* A16;      // m x k_pitch 16-bit operand (f16 for int8 problems, bf16 otherwise)
     const void* B16;      // n x k_pitch 16-bit operand
@@ -60,17 +85,26 @@ struct TcLaunch {
     int grid;
     int chunk_kb;         // k-blocks accumulated in TMEM before a drain
     bool int_out;         // true: int8 problem (f16 operands, int32 output)
+    int split_k;          // K slices of the tail tiles (1 = none)
+    int64_t split_from;   // first split tile
+    int* split_flags;     // (tiles - split_from) * kTcEpilogueWarps ints, zeroed (device)
+    uint32_t epoch;       // launch epoch written to / awaited in split_flags
 };
 
 cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream);
+// block_per_cu of a tile as the planner counts it (registers, shared memory,
+// TMEM); the tail split is used only when the whole grid fits at once.
+int tc_blocks_per_sm(int bm, int bn);
 // Occupancy of one kernel instance (CTAs per SM) as the runtime reports it.
 int tc_occupancy(int bm, int bn, bool int_out);
 int tc_num_regs(int bm, int bn, bool int_out);
 
 // ---- operand staging (stage.cu) --------------------------------------------
 // int8 -> f16 (exact), row pitch k -> k_pitch, for A (m rows) and Bt (n rows).
+// Also zeroes `zero_count` ints at `zero` (the tail-split flags), if any.
 cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
-                            int64_t n, int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream);
+                            int64_t n, int64_t k, int64_t k_pitch, int* zero, int64_t zero_count, int num_sms,
+                            cudaStream_t stream);
 // 16-bit copy with row pitch k -> k_pitch (bf16 problems whose k is not a
 // multiple of 8).
 cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,

@@ -124,7 +124,7 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;
     uint16_t* Ah = reinterpret_cast<uint16_t*>(d->scratch);
     uint16_t* Bh = reinterpret_cast<uint16_t*>(d->scratch + round256(p->m * p->k_pitch * 2));
-    if (launch_stage_i8(A, Bt, Ah, Bh, p->m, p->n, p->k, p->k_pitch, d->num_sms, stream) != cudaSuccess)
+    if (launch_stage_i8(A, Bt, Ah, Bh, p->m, p->n, p->k, p->k_pitch, nullptr, 0, d->num_sms, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     TcLaunch L;
     L.A16 = Ah;
@@ -140,5 +140,9 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     L.grid = p->grid;
     L.chunk_kb = p->chunk_k / kTcBK;
     L.int_out = true;
+    L.split_k = 1;   // no tail split: its flags would need device memory
+    L.split_from = 0;
+    L.split_flags = nullptr;
+    L.epoch = 0;
     return launch_tc(L, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -68,6 +68,8 @@ int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 }  // namespace
 
+int tc_blocks_per_sm(int bm, int bn) { return tile_bpc(Tile{bm, bn}); }
+
 gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t num_sms, gemm_plan* out) {
     if (!out) return GEMM_ERR_INVALID_ARG;
     if (dtype != GEMM_DTYPE_I8 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
@@ -100,6 +102,8 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
         p.chunk_k = static_cast<int32_t>(k);
         p.ratio = 2.0 * m / (m + 1.0);  // flops per byte streamed (m rows of A reused per Bt byte)
         p.workspace_bytes = 0;
+        p.split_k = 1;
+        p.split_from = p.tiles;
         *out = p;
         return GEMM_OK;
     }
@@ -189,6 +193,11 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
         p.chunk_k = static_cast<int32_t>(num_kb * kTcBK > kMaxDim ? kMaxDim : num_kb * kTcBK);
         p.workspace_bytes = (k % 8 == 0) ? 0 : round_up(m * k_pitch * 2, 256) + round_up(n * k_pitch * 2, 256);
     }
+    // Beyond the five steps: split the last, partial wave along K.
+    const int64_t nchunks = ceil_div(num_kb, p.chunk_k / kTcBK);
+    int64_t split_from = tiles;
+    p.split_k = tc_tail_split(tiles, p.grid, nchunks, dtype == GEMM_DTYPE_I8, &split_from);
+    p.split_from = static_cast<int32_t>(split_from);
     *out = p;
     return GEMM_OK;
 }

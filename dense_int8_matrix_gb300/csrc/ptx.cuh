@@ -20,6 +20,7 @@ enum DeviceErrorCode : int {
     kDevErrTimeoutEpilogue = 3,   // epilogue waited too long for an accumulator
     kDevErrTimeoutTeardown = 4,   // teardown waited too long for in-flight copies / MMAs
     kDevErrTimeoutSelfTest = 5,   // the self-test's wait on a barrier nothing completes
+    kDevErrTimeoutSplit = 6,      // a split-tile slice waited too long for slice 0's stores
 };
 
 // One wait gives up after this many nanoseconds of %globaltimer time, or after
@@ -115,6 +116,20 @@ __device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int
                      reinterpret_cast<uint64_t>(desc)),
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
+}
+
+// 2-D tiled reduce-add of one box from shared memory into global memory
+// (element type from the tensor map; integer addition is exact).
+__device__ __forceinline__ void tma_reduce_add_2d(const void* desc, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(desc)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+// Order generic-proxy global accesses with async-proxy (TMA) ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

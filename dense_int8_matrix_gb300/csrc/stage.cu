@@ -61,9 +61,12 @@ constexpr int kStageUnroll = 4;
 __global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restrict__ srcA,
                                                             const uint4* __restrict__ srcB, uint4* __restrict__ dstA,
                                                             uint4* __restrict__ dstB, int64_t itemsA,
-                                                            int64_t itemsB) {
+                                                            int64_t itemsB, int* __restrict__ zero,
+                                                            int64_t zero_count) {
     const int64_t total = itemsA + itemsB;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_count; i += stride)
+        zero[i] = 0;
     for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
          i0 += stride * kStageUnroll) {
         uint4 v[kStageUnroll];
@@ -84,10 +87,13 @@ __global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restr
 __global__ void __launch_bounds__(256) stage_i8_rows_kernel(const int8_t* __restrict__ A,
                                                             const int8_t* __restrict__ Bt, __half* __restrict__ Ah,
                                                             __half* __restrict__ Bh, int64_t m, int64_t n, int64_t k,
-                                                            int64_t k_pitch) {
+                                                            int64_t k_pitch, int* __restrict__ zero,
+                                                            int64_t zero_count) {
     const int64_t totalA = m * k;
     const int64_t total = totalA + n * k;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_count; i += stride)
+        zero[i] = 0;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
         const bool isA = i < totalA;
         const int64_t j = isA ? i : i - totalA;
@@ -125,7 +131,8 @@ int grid_for(int64_t items, int num_sms) {
 }  // namespace
 
 cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m, int64_t n,
-                            int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream) {
+                            int64_t k, int64_t k_pitch, int* zero, int64_t zero_count, int num_sms,
+                            cudaStream_t stream) {
     const bool aligned = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bt) |
                            reinterpret_cast<uintptr_t>(Ah) | reinterpret_cast<uintptr_t>(Bh)) &
                           15u) == 0;
@@ -133,10 +140,10 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
         const int64_t itemsA = m * k / 16, itemsB = n * k / 16;
         stage_i8_flat_kernel<<<grid_for(itemsA + itemsB, num_sms), 256, 0, stream>>>(
             reinterpret_cast<const uint4*>(A), reinterpret_cast<const uint4*>(Bt), reinterpret_cast<uint4*>(Ah),
-            reinterpret_cast<uint4*>(Bh), itemsA, itemsB);
+            reinterpret_cast<uint4*>(Bh), itemsA, itemsB, zero, zero_count);
     } else {
         stage_i8_rows_kernel<<<grid_for((m + n) * k, num_sms), 256, 0, stream>>>(
-            A, Bt, reinterpret_cast<__half*>(Ah), reinterpret_cast<__half*>(Bh), m, n, k, k_pitch);
+            A, Bt, reinterpret_cast<__half*>(Ah), reinterpret_cast<__half*>(Bh), m, n, k, k_pitch, zero, zero_count);
     }
     return cudaGetLastError();
 }

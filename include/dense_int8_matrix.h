@@ -60,12 +60,20 @@ enum {
     GEMM_KERNEL_KINDS = 3
 };
 
-#define GEMM_PLAN_VERSION 1
+#define GEMM_PLAN_VERSION 2
 #define GEMM_I8_MAX_K 131071 /* 131071 * 128 * 128 < 2^31 */
 
 /*
  * The selected configuration (patent CN114238853A claim 7: "input the size,
  * select the configuration and its kernel, run").  Filled by gemm_*_plan.
+ *
+ * Tail split (an addition to the patent's five steps, int8 only): when the
+ * tiles do not fill a whole number of waves, the tiles of the last, partial
+ * wave are split along K into split_k slices run by otherwise idle CTAs.
+ * Slice 0 stores its int32 partial sums; the other slices add theirs with
+ * TMA reduce-add once slice 0's stores are complete.  Integer addition is
+ * exact and order-free, so the result is bit-identical to the unsplit one.
+ * gemm_*_run recomputes the split for the tile and grid it actually launches.
  */
 typedef struct gemm_plan {
     int32_t version;   /* GEMM_PLAN_VERSION */
@@ -82,10 +90,12 @@ typedef struct gemm_plan {
     int32_t k_pitch;     /* row pitch (elements) of the staged 16-bit operands */
     int32_t chunk_k;     /* K elements accumulated in fp32 before an exact int32 drain */
     int32_t fallback;    /* 1 if no tile filled the chip (claim 4 S3) */
-    int32_t reserved0;
+    int32_t split_k;     /* K slices of each tile in the last, partial wave (1 = none) */
     double ratio;        /* compute-to-memory ratio of the tile (claim 5), flop per byte */
     int64_t workspace_bytes; /* device scratch gemm_*_run takes from its pool */
-    int64_t reserved[4];
+    int32_t split_from;  /* tiles [split_from, tiles) are split into split_k K slices */
+    int32_t reserved0;
+    int64_t reserved[3];
 } gemm_plan;
 
 /*

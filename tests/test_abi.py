@@ -157,6 +157,35 @@ def test_status_strings(lib):
     assert B.gemm_status_string(42) == "GEMM_ERR_UNKNOWN"
 
 
+@pytest.mark.parametrize("m,k,n,sms,split,split_from", [
+    (4096, 4096, 4096, 152, 2, 456),     # 512 tiles: 3 whole waves + 56 tiles in 2 K slices
+    (4096, 4096, 4096, 148, 2, 444),     # 512 = 3 * 148 + 68; 148 // 68 = 2
+    (8192, 8192, 8192, 152, 2, 1976),    # 2048 = 13 * 152 + 72
+    (8192, 8192, 8192, 148, 1, 2048),    # 2048 = 13 * 148 + 124 -> 148 // 124 = 1: no split
+    (1000, 777, 3000, 148, 1, 192),      # one K chunk: nothing to split
+    (4096, 4096, 4096 + 256 * 11, 152, 1, 0),
+])
+def test_tail_split_fields(lib, m, k, n, sms, split, split_from):
+    p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, m, k, n, sms)
+    tiles = p.tiles
+    full = (tiles // p.grid) * p.grid
+    tail = tiles - full
+    want = 1
+    if tiles > p.grid and tail:
+        nch = -(-(-(-k // 64)) // 16)
+        want = min(p.grid // tail, nch, 8)
+        if want < 2:
+            want = 1
+    assert p.split_k == want
+    if want > 1:
+        assert (p.split_k, p.split_from) == (split, split_from)
+        assert p.split_from + (tiles - p.split_from) * p.split_k <= full + p.grid
+    else:
+        assert p.split_from == tiles
+    pb = B.gemm_plan_for_sms(B.GEMM_DTYPE_BF16, m, k, n, sms)
+    assert pb.split_k == 1 and pb.split_from == pb.tiles
+
+
 def test_skinny_plan_fields(lib):
     p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 64, 8192, 8192, 148)
     assert p.path == B.GEMM_PATH_SKINNY and p.grid == 256 and p.workspace_bytes == 0

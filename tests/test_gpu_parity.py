@@ -276,3 +276,38 @@ def test_bounded_wait_gives_up_and_reports():
     A = workloads.random_i8((256, 300), 31)
     Bt = workloads.random_i8((200, 300), 32)
     G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
+
+
+@pytest.mark.parametrize("grid,n,split", [
+    (14, 1000, 3),    # 32 tiles = 2 x 14 + 4 -> 4 tiles in 3 K slices (TMA reduce-add)
+    (10, 1000, 5),    # 30 + 2 -> 2 tiles in 5 slices of one chunk each
+    (31, 1000, 5),    # 31 + 1 -> 1 tile in 5 slices
+    (13, 998, 2),     # n % 4 != 0: direct stores and atomic adds
+])
+def test_i8_tail_split_exact(grid, n, split):
+    # int8 tiles of the last, partial wave split along K: slice 0 stores,
+    # the others add after it; the result must stay bit-exact
+    m, k = 1000, 4100
+    A = workloads.random_i8((m, k), 41)
+    Bt = workloads.random_i8((n, k), 42)
+    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, 128, 256, grid)
+    tiles = -(-m // 128) * -(-n // 256)
+    full = tiles // grid * grid
+    assert min(grid // (tiles - full), 5, 8) == split
+    C1 = G.gpu_i8(A, Bt, plan=p)
+    G.assert_i8_exact(A, Bt, C1)
+    C2 = G.gpu_i8(A, Bt, plan=p)    # again: the flags start from zero every launch
+    assert torch.equal(C1, C2)
+
+
+def test_i8_tail_split_workloads_extreme():
+    # 4096^3 runs 56 tail tiles in 2 K slices on 152 SMs; extreme values
+    # check that the slice sums add exactly
+    m = k = n = 4096
+    A = torch.full((m, k), -128, dtype=torch.int8)
+    Bt = torch.full((n, k), -128, dtype=torch.int8)
+    Bt[::3] = 127
+    C = G.gpu_i8(A, Bt)
+    want = torch.full((n,), 16384 * k, dtype=torch.int32)
+    want[::3] = -128 * 127 * k
+    assert torch.equal(C, want.expand(m, n))
