@@ -122,6 +122,26 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     if (!tensor_map_encoder_available() && p->path == GEMM_PATH_TENSOR) return GEMM_ERR_CUDA;
 
     if (p->path == GEMM_PATH_SKINNY) {
+        if (skinny_tc_supported(p->m, p->n, p->k, A, Bt) && tensor_map_encoder_available()) {
+            // f16 copy of the small activation matrix; the same launch zeroes C,
+            // which the tensor-core kernel adds its partial sums into
+            void* ws = nullptr;
+            const size_t a_bytes = static_cast<size_t>(p->m * p->k * 2);
+            if (cudaMallocFromPoolAsync(&ws, a_bytes, ds->pool, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+            cudaError_t e;
+            {
+                TraceScope t(GEMM_KERNEL_STAGE, stream);
+                e = launch_stage_i8(static_cast<const int8_t*>(A), nullptr, static_cast<uint16_t*>(ws), nullptr, p->m, 0,
+                                    p->k, p->k, static_cast<int*>(C), p->m * p->n, ds->num_sms, stream);
+            }
+            if (e == cudaSuccess) {
+                TraceScope t(GEMM_KERNEL_SKINNY, stream);
+                e = launch_skinny_tc(static_cast<const int8_t*>(Bt), static_cast<const uint16_t*>(ws),
+                                     static_cast<int32_t*>(C), ds->err_word, p->m, p->n, p->k, ds->num_sms, stream);
+            }
+            cudaFreeAsync(ws, stream);
+            return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+        }
         TraceScope t(GEMM_KERNEL_SKINNY, stream);
         if (launch_skinny_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), static_cast<int32_t*>(C),
                              p->m, p->n, p->k, ds->num_sms, stream) != cudaSuccess)

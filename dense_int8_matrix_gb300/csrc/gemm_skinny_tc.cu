@@ -1,0 +1,387 @@
+// Skinny int8 GEMM on the tensor cores (m <= 64): C = A x B with B stored
+// K-major as Bt (n x k).  Bt (n*k bytes) dwarfs A and C, so the kernel's job is
+// to stream Bt from HBM once, at full bandwidth; the patent CN114238853A
+// (claim 4 S3) calls such shapes too small to fill the chip with output tiles.
+//
+// Computed as C^T = Bt x A^T ("swap AB"): the MMA's M side is 128 rows of Bt,
+// its N side is m padded to NP in {16, 32, 64}, fp32 accumulation in TMEM,
+// drained to exact int32 every 1024 K elements as in the large kernel.
+//
+// Data path per 64-element K step, per CTA (12 warps):
+//   warp 0      TMA: the int8 Bt box (64 B x 128 rows, 64-byte swizzle) and
+//               the f16 activation box (64 x NP, 128-byte swizzle) into one
+//               stage of an 8-deep shared-memory ring;
+//   warps 4-7   widen: each lane reads its Bt row (64 int8) from shared
+//               memory, widens it to f16 in registers (exact) and writes it
+//               with tcgen05.st into one of four TMEM operand buffers: the
+//               MMA reads its A operand from TMEM, so shared memory carries
+//               only the int8 bytes (read once) and the small activation tile;
+//   warp 1      tcgen05.mma (A from TMEM, B = activations from shared memory)
+//               into one of two TMEM accumulators;
+//   warps 8-11  drain the accumulator to int32 running sums and, at the end
+//               of each run of K steps of one 128-row tile, add them into C
+//               (pre-zeroed) with coalesced integer atomics: exact and
+//               order-free.
+// Work split ("stream-K"): the (row tile, K step) iterations are numbered
+// tile-major and every CTA takes an equal contiguous range, so all SMs
+// stream the same number of Bt bytes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gemm {
+
+namespace {
+
+constexpr int kSkStages = 8;
+constexpr int kSkBtBytes = 128 * 64;       // int8 Bt box per stage
+constexpr int kSkAbufs = 4;                // TMEM operand buffers (32 columns each)
+constexpr int kSkThreads = 384;
+constexpr int kSkChunkKb = kI8ChunkK / 64; // K steps per exact fp32 chunk
+
+template <int NP>
+struct SkCfg {
+    static constexpr int ACT_BYTES = NP * 128;                 // f16 activation box per stage
+    static constexpr int STAGE_BYTES = kSkBtBytes + ACT_BYTES;  // multiple of 1024
+    static constexpr int TMEM_COLS = 256;                      // 4 x 32 operand + 2 x NP accumulator
+    static constexpr size_t SMEM = static_cast<size_t>(kSkStages) * STAGE_BYTES + 1024 + 1024;
+    static_assert(kSkAbufs * 32 + 2 * NP <= TMEM_COLS, "TMEM budget");
+};
+
+struct SkParams {
+    int32_t* C;
+    int* err;
+    int m, n;
+    int num_kb;       // K steps of 64
+    int tiles;        // ceil(n / 128)
+    int64_t iters;    // tiles * num_kb
+};
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// two int8 of a (x ^ 0x80)-biased word -> two exact f16 (see stage.cu)
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t biased, uint32_t selector) {
+    uint32_t packed = __byte_perm(biased, 0x64646464u, selector);
+    uint32_t out;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(packed), "r"(0x64806480u));
+    return out;
+}
+
+// The iteration range of one CTA and the chunk structure inside it: a chunk
+// ends after a K step that closes 16 K steps of a tile, the tile, or the range.
+__device__ __forceinline__ void cta_range(const SkParams& p, int64_t& lo, int64_t& hi) {
+    lo = p.iters * blockIdx.x / gridDim.x;
+    hi = p.iters * (blockIdx.x + 1) / gridDim.x;
+}
+
+__device__ __forceinline__ bool chunk_ends(const SkParams& p, int64_t i, int64_t hi) {
+    const int kb = static_cast<int>(i % p.num_kb);
+    return (i + 1 == hi) || (kb + 1 == p.num_kb) || ((kb + 1) % kSkChunkKb == 0);
+}
+
+__device__ __forceinline__ bool segment_ends(const SkParams& p, int64_t i, int64_t hi) {
+    const int kb = static_cast<int>(i % p.num_kb);
+    return (i + 1 == hi) || (kb + 1 == p.num_kb);
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    skinny_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
+                     const SkParams p) {
+    using Cfg = SkCfg<NP>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* ctrl = smem_raw + (base - raw) + kSkStages * Cfg::STAGE_BYTES;
+    const uint32_t bar0 = smem_u32(ctrl);
+    const uint32_t full0 = bar0;                          // [kSkStages]
+    const uint32_t empty0 = full0 + 8u * kSkStages;       // [kSkStages]
+    const uint32_t aready0 = empty0 + 8u * kSkStages;     // [kSkAbufs]
+    const uint32_t afree0 = aready0 + 8u * kSkAbufs;      // [kSkAbufs]
+    const uint32_t accf0 = afree0 + 8u * kSkAbufs;        // [2]
+    const uint32_t acce0 = accf0 + 16u;                   // [2]
+    const uint32_t done_bar = acce0 + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kSkStages + 2 * kSkAbufs + 5));
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kSkStages; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 4 + 1);   // four widening warps + the MMA's commit
+        }
+        for (int b = 0; b < kSkAbufs; ++b) {
+            mbar_init(aready0 + 8u * b, 4);
+            mbar_init(afree0 + 8u * b, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8u * b, 1);
+            mbar_init(acce0 + 8u * b, 4);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_acc = tmem_base + kSkAbufs * 32;   // two accumulators of NP columns
+
+    int64_t lo, hi;
+    cta_range(p, lo, hi);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA --
+        if (lane == 0) {
+            tma_prefetch_desc(&tmB);
+            tma_prefetch_desc(&tmA);
+            const uint64_t pol_stream = policy_evict_first();
+            const uint64_t pol_keep = policy_evict_last();
+            uint32_t n_iss = 0;
+            for (int64_t i = lo; i < hi; ++i, ++n_iss) {
+                const uint32_t s = n_iss % kSkStages, ph = (n_iss / kSkStages) & 1u;
+                if (!wait_bounded(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) break;
+                const int tile = static_cast<int>(i / p.num_kb);
+                const int kb = static_cast<int>(i % p.num_kb);
+                const uint32_t st = base + s * Cfg::STAGE_BYTES;
+                mbar_arrive_expect_tx(full0 + 8u * s, Cfg::STAGE_BYTES);
+                tma_load_2d(st, &tmB, kb * 64, tile * 128, full0 + 8u * s, pol_stream);
+                tma_load_2d(st + kSkBtBytes, &tmA, kb * 64, 0, full0 + 8u * s, pol_keep);
+            }
+            for (uint32_t s = 0; s < static_cast<uint32_t>(kSkStages) && s < n_iss; ++s) {
+                const uint32_t last = s + ((n_iss - 1u - s) / kSkStages) * kSkStages;
+                wait_bounded(full0 + 8u * s, (last / kSkStages) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA --
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(0u, 128, NP);
+            uint32_t n = 0, chunk_iter = 0;
+            bool ok = true;
+            bool chunk_open = false;
+            uint32_t d_tmem = tmem_acc;
+            uint32_t first = 1;
+            for (int64_t i = lo; ok && i < hi; ++i, ++n) {
+                if (!chunk_open) {
+                    const uint32_t buf = chunk_iter & 1u, aph = (chunk_iter >> 1) & 1u;
+                    if (!wait_bounded(acce0 + 8u * buf, aph ^ 1u, abort_flag, p.err, kDevErrTimeoutMma)) break;
+                    d_tmem = tmem_acc + buf * NP;
+                    chunk_open = true;
+                    first = 1;
+                }
+                const uint32_t s = n % kSkStages, ph = (n / kSkStages) & 1u;
+                const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
+                if (!wait_bounded(full0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutMma)) break;
+                if (!wait_bounded(aready0 + 8u * b, bph, abort_flag, p.err, kDevErrTimeoutMma)) break;
+                tc_fence_after();
+                const uint64_t bdesc = smem_desc_sw128_kmajor(base + s * Cfg::STAGE_BYTES + kSkBtBytes);
+                const uint32_t a_tmem = tmem_base + b * 32;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc + 2u * kk, idesc, (first == 0 || kk > 0) ? 1u : 0u);
+                }
+                first = 0;
+                mma_commit(afree0 + 8u * b);
+                mma_commit(empty0 + 8u * s);
+                if (chunk_ends(p, i, hi)) {
+                    mma_commit(accf0 + 8u * (chunk_iter & 1u));
+                    ++chunk_iter;
+                    chunk_open = false;
+                }
+            }
+            mma_commit(done_bar);
+            wait_bounded(done_bar, 0u, nullptr, p.err, kDevErrTimeoutTeardown);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------------- widen --
+        const int q = warp & 3;
+        const int row = q * 32 + lane;            // row of the 128-row Bt box
+        const uint32_t swz = (row >> 1) & 3;      // 64-byte swizzle of this row
+        uint32_t n = 0;
+        for (int64_t i = lo; i < hi; ++i, ++n) {
+            const uint32_t s = n % kSkStages, ph = (n / kSkStages) & 1u;
+            const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
+            int got = 1;
+            if (lane == 0) {
+                got = wait_bounded(full0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutEpilogue) &&
+                      wait_bounded(afree0 + 8u * b, bph ^ 1u, abort_flag, p.err, kDevErrTimeoutEpilogue);
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) break;
+            tc_fence_after();
+            const uint32_t src = base + s * Cfg::STAGE_BYTES + row * 64;
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 v = ld_shared_v4(src + ((c ^ swz) << 4));
+                const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u;
+                const uint32_t x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;
+                w[8 * c + 0] = i8x2_to_f16x2(x0, 0x4140u);
+                w[8 * c + 1] = i8x2_to_f16x2(x0, 0x4342u);
+                w[8 * c + 2] = i8x2_to_f16x2(x1, 0x4140u);
+                w[8 * c + 3] = i8x2_to_f16x2(x1, 0x4342u);
+                w[8 * c + 4] = i8x2_to_f16x2(x2, 0x4140u);
+                w[8 * c + 5] = i8x2_to_f16x2(x2, 0x4342u);
+                w[8 * c + 6] = i8x2_to_f16x2(x3, 0x4140u);
+                w[8 * c + 7] = i8x2_to_f16x2(x3, 0x4342u);
+            }
+            tmem_st_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 32, w);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(aready0 + 8u * b);
+                mbar_arrive(empty0 + 8u * s);
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------- epilogue --
+        const int q = warp & 3;
+        const int jrow = q * 32 + lane;           // TMEM lane = row of the Bt tile = column j of C
+        int32_t sum[NP];
+#pragma unroll
+        for (int c = 0; c < NP; ++c) sum[c] = 0;
+        uint32_t chunk_iter = 0;
+        for (int64_t i = lo; i < hi; ++i) {
+            if (!chunk_ends(p, i, hi)) continue;
+            const uint32_t buf = chunk_iter & 1u, aph = (chunk_iter >> 1) & 1u;
+            int got = 1;
+            if (lane == 0) got = wait_bounded(accf0 + 8u * buf, aph, abort_flag, p.err, kDevErrTimeoutEpilogue);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_acc + buf * NP + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+            for (int c0 = 0; c0 < NP; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(taddr + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) sum[c0 + c] += __float2int_rn(__uint_as_float(v[c]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce0 + 8u * buf);
+            ++chunk_iter;
+            if (segment_ends(p, i, hi)) {
+                const int64_t j = static_cast<int64_t>(i / p.num_kb) * 128 + jrow;
+                if (j < p.n) {
+#pragma unroll
+                    for (int c = 0; c < NP; ++c)
+                        if (c < p.m) atomicAdd(p.C + static_cast<int64_t>(c) * p.n + j, sum[c]);
+                }
+#pragma unroll
+                for (int c = 0; c < NP; ++c) sum[c] = 0;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+template <int NP>
+cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* err, int64_t m, int64_t n, int64_t k,
+                      int num_sms, cudaStream_t stream) {
+    using Cfg = SkCfg<NP>;
+    auto enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!enc) return cudaErrorInvalidValue;
+    CUtensorMap mB, mA;
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(n)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
+        cuuint32_t box[2] = {64u, 128u};
+        cuuint32_t estr[2] = {1u, 1u};
+        if (enc(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(Bt), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2u};
+        cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(NP)};
+        cuuint32_t estr[2] = {1u, 1u};
+        if (enc(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(A16), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    SkParams p;
+    p.C = C;
+    p.err = err;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.num_kb = static_cast<int>((k + 63) / 64);
+    p.tiles = static_cast<int>((n + 127) / 128);
+    p.iters = static_cast<int64_t>(p.tiles) * p.num_kb;
+    int64_t grid = num_sms;
+    if (grid > p.iters) grid = p.iters;
+    auto kern = skinny_tc_kernel<NP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM));
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(grid), kSkThreads, Cfg::SMEM, stream>>>(mB, mA, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool skinny_tc_supported(int64_t m, int64_t n, int64_t k, const void* A, const void* Bt) {
+    return m >= 1 && m <= 64 && (k % 16) == 0 && n <= 2147483647LL - 128 &&
+           ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bt)) & 15u) == 0;
+}
+
+cudaError_t launch_skinny_tc(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* err, int64_t m, int64_t n,
+                             int64_t k, int num_sms, cudaStream_t stream) {
+    if (m <= 16) return launch_np<16>(Bt, A16, C, err, m, n, k, num_sms, stream);
+    if (m <= 32) return launch_np<32>(Bt, A16, C, err, m, n, k, num_sms, stream);
+    return launch_np<64>(Bt, A16, C, err, m, n, k, num_sms, stream);
+}
+
+}  // namespace gemm

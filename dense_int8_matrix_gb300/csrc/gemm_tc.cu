@@ -562,6 +562,8 @@ const void* find_kernel(int bm, int bn, bool int_out) {
 
 bool tensor_map_encoder_available() { return get_encoder() != nullptr; }
 
+void* tensor_map_encoder() { return reinterpret_cast<void*>(get_encoder()); }
+
 cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream) {
     return a.int_out ? dispatch<true>(a, stream) : dispatch<false>(a, stream);
 }

@@ -110,7 +110,15 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
 cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
                              int64_t n, int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream);
 
-// ---- skinny path (gemm_skinny.cu) -------------------------------------------
+// ---- skinny path on the tensor cores (gemm_skinny_tc.cu) --------------------
+// Needs k % 16 == 0 (TMA row pitch of int8 Bt) and 16-byte aligned A and Bt.
+bool skinny_tc_supported(int64_t m, int64_t n, int64_t k, const void* A, const void* Bt);
+// A16: the m x k activations as f16 (row pitch k); C must be zero (the kernel
+// adds its partial sums into it).
+cudaError_t launch_skinny_tc(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* err, int64_t m, int64_t n,
+                             int64_t k, int num_sms, cudaStream_t stream);
+
+// ---- skinny path on CUDA cores (gemm_skinny.cu) -----------------------------
 cudaError_t launch_skinny_i8(const int8_t* A, const int8_t* Bt, int32_t* C, int64_t m, int64_t n, int64_t k,
                              int num_sms, cudaStream_t stream);
 
@@ -121,5 +129,6 @@ cudaError_t launch_selftest_wait(int* err, uint64_t timeout_ns, cudaStream_t str
 
 // ---- driver entry point for tensor-map encoding (gemm_tc.cu) ----------------
 bool tensor_map_encoder_available();
+void* tensor_map_encoder();   // cuTensorMapEncodeTiled, or nullptr
 
 }  // namespace gemm

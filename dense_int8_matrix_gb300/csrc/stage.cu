@@ -138,7 +138,8 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
                           15u) == 0;
     if (k == k_pitch && (k % 16) == 0 && aligned) {
         const int64_t itemsA = m * k / 16, itemsB = n * k / 16;
-        stage_i8_flat_kernel<<<grid_for(itemsA + itemsB, num_sms), 256, 0, stream>>>(
+        const int64_t work = itemsA + itemsB > zero_count / 4 ? itemsA + itemsB : zero_count / 4;
+        stage_i8_flat_kernel<<<grid_for(work, num_sms), 256, 0, stream>>>(
             reinterpret_cast<const uint4*>(A), reinterpret_cast<const uint4*>(Bt), reinterpret_cast<uint4*>(Ah),
             reinterpret_cast<uint4*>(Bh), itemsA, itemsB, zero, zero_count);
     } else {

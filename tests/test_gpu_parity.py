@@ -243,7 +243,7 @@ def test_trace_counts_launches():
     B.gemm_trace_begin(4)
     B.gemm_i8_run(ps, dA[:16].contiguous(), dB, C[:16].contiguous())
     ms, cnt = B.gemm_trace_collect()
-    assert cnt == [0, 0, 1]
+    assert cnt == [1, 0, 1]     # f16 copy of A (and zeroing of C), then the skinny kernel
 
 
 @pytest.mark.parametrize("bm,bn", TILES)
@@ -311,3 +311,25 @@ def test_i8_tail_split_workloads_extreme():
     want = torch.full((n,), 16384 * k, dtype=torch.int32)
     want[::3] = -128 * 127 * k
     assert torch.equal(C, want.expand(m, n))
+
+
+@pytest.mark.parametrize("m,k,n", [
+    (1, 16, 1), (16, 64, 128), (17, 4112, 300), (33, 2048, 129), (64, 1040, 1000),
+    (5, 20000, 640), (40, 8192, 8191), (64, 128, 40000),
+])
+def test_i8_skinny_tensor_core_shapes(m, k, n):
+    # k % 16 == 0: the tensor-core skinny kernel (stream-K over 128-row tiles,
+    # int8 widened into TMEM, exact int32 atomics into C)
+    A = workloads.random_i8((m, k), m + k)
+    Bt = workloads.random_i8((n, k), n + 2 * k)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
+
+
+def test_i8_skinny_extremes():
+    m, k, n = 64, 16384, 1000
+    A = torch.full((m, k), -128, dtype=torch.int8)
+    Bt = torch.full((n, k), -128, dtype=torch.int8)
+    Bt[1::2] = 127
+    C = G.gpu_i8(A, Bt)
+    assert torch.all(C[:, 0::2] == 16384 * k)
+    assert torch.all(C[:, 1::2] == -128 * 127 * k)
