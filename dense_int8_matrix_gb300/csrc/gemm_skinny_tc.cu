@@ -7,21 +7,23 @@
 // its N side is m padded to NP in {16, 32, 64}, fp32 accumulation in TMEM,
 // drained to exact int32 every 1024 K elements as in the large kernel.
 //
-// Data path per 64-element K step, per CTA (12 warps):
+// Data path per 64-element K step, per CTA (28 warps):
 //   warp 0      TMA: the int8 Bt box (64 B x 128 rows, 64-byte swizzle) and
 //               the f16 activation box (64 x NP, 128-byte swizzle) into one
-//               stage of an 8-deep shared-memory ring;
-//   warps 4-7   widen: each lane reads its Bt row (64 int8) from shared
-//               memory, widens it to f16 in registers (exact) and writes it
-//               with tcgen05.st into one of four TMEM operand buffers: the
-//               MMA reads its A operand from TMEM, so shared memory carries
-//               only the int8 bytes (read once) and the small activation tile;
+//               stage of a 12-16-deep shared-memory ring;
+//   warps 4-19  widen, in four groups of four warps that take the K steps in
+//               turn (one warp of a group per TMEM lane quarter): each lane
+//               reads its Bt row (64 int8) from shared memory, widens it to
+//               f16 in registers (exact) and writes it with tcgen05.st into
+//               one of eight TMEM operand buffers.  The MMA reads its A
+//               operand from TMEM, so shared memory carries only the int8
+//               bytes (read once) and the small activation tile;
 //   warp 1      tcgen05.mma (A from TMEM, B = activations from shared memory)
 //               into one of two TMEM accumulators;
-//   warps 8-11  drain the accumulator to int32 running sums and, at the end
-//               of each run of K steps of one 128-row tile, add them into C
-//               (pre-zeroed) with coalesced integer atomics: exact and
-//               order-free.
+//   warps 20-27 drain each accumulator chunk (two warps per lane quarter,
+//               half of the NP columns each), convert it to int32 (exact) and
+//               add it into C (pre-zeroed) with coalesced integer atomics:
+//               exact and order-free.
 // Work split ("stream-K"): the (row tile, K step) iterations are numbered
 // tile-major and every CTA takes an equal contiguous range, so all SMs
 // stream the same number of Bt bytes.
@@ -37,19 +39,25 @@ namespace gemm {
 
 namespace {
 
-constexpr int kSkStages = 8;
 constexpr int kSkBtBytes = 128 * 64;       // int8 Bt box per stage
-constexpr int kSkAbufs = 4;                // TMEM operand buffers (32 columns each)
-constexpr int kSkThreads = 384;
+constexpr int kSkGroups = 4;               // widening groups (4 warps each)
+constexpr int kSkAbufs = 2 * kSkGroups;    // TMEM operand buffers (32 columns each)
+constexpr int kSkEpiWarps = 8;
+constexpr int kSkWidenWarp0 = 4;
+constexpr int kSkEpiWarp0 = kSkWidenWarp0 + 4 * kSkGroups;
+constexpr int kSkThreads = 32 * (kSkEpiWarp0 + kSkEpiWarps);   // 896
 constexpr int kSkChunkKb = kI8ChunkK / 64; // K steps per exact fp32 chunk
 
 template <int NP>
 struct SkCfg {
     static constexpr int ACT_BYTES = NP * 128;                 // f16 activation box per stage
     static constexpr int STAGE_BYTES = kSkBtBytes + ACT_BYTES;  // multiple of 1024
-    static constexpr int TMEM_COLS = 256;                      // 4 x 32 operand + 2 x NP accumulator
-    static constexpr size_t SMEM = static_cast<size_t>(kSkStages) * STAGE_BYTES + 1024 + 1024;
+    static constexpr int STAGES = NP >= 64 ? 12 : 16;
+    static constexpr int TMEM_COLS = 512;                      // 8 x 32 operand + 2 x NP accumulator
+    static constexpr int EPI_COLS = NP / 2;                    // columns per epilogue warp
+    static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 1024;
     static_assert(kSkAbufs * 32 + 2 * NP <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM <= 232448, "shared memory");
 };
 
 struct SkParams {
@@ -61,16 +69,19 @@ struct SkParams {
     int64_t iters;    // tiles * num_kb
 };
 
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -111,11 +122,6 @@ __device__ __forceinline__ bool chunk_ends(const SkParams& p, int64_t i, int64_t
     return (i + 1 == hi) || (kb + 1 == p.num_kb) || ((kb + 1) % kSkChunkKb == 0);
 }
 
-__device__ __forceinline__ bool segment_ends(const SkParams& p, int64_t i, int64_t hi) {
-    const int kb = static_cast<int>(i % p.num_kb);
-    return (i + 1 == hi) || (kb + 1 == p.num_kb);
-}
-
 template <int NP>
 __global__ void __launch_bounds__(kSkThreads, 1)
     skinny_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
@@ -124,25 +130,25 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* ctrl = smem_raw + (base - raw) + kSkStages * Cfg::STAGE_BYTES;
+    uint8_t* ctrl = smem_raw + (base - raw) + Cfg::STAGES * Cfg::STAGE_BYTES;
     const uint32_t bar0 = smem_u32(ctrl);
-    const uint32_t full0 = bar0;                          // [kSkStages]
-    const uint32_t empty0 = full0 + 8u * kSkStages;       // [kSkStages]
-    const uint32_t aready0 = empty0 + 8u * kSkStages;     // [kSkAbufs]
+    const uint32_t full0 = bar0;                          // [Cfg::STAGES]
+    const uint32_t empty0 = full0 + 8u * Cfg::STAGES;       // [Cfg::STAGES]
+    const uint32_t aready0 = empty0 + 8u * Cfg::STAGES;     // [kSkAbufs]
     const uint32_t afree0 = aready0 + 8u * kSkAbufs;      // [kSkAbufs]
     const uint32_t accf0 = afree0 + 8u * kSkAbufs;        // [2]
     const uint32_t acce0 = accf0 + 16u;                   // [2]
     const uint32_t done_bar = acce0 + 16u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kSkStages + 2 * kSkAbufs + 5));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * Cfg::STAGES + 2 * kSkAbufs + 5));
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < kSkStages; ++s) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, 4 + 1);   // four widening warps + the MMA's commit
+            mbar_init(empty0 + 8u * s, 4 + 1);   // the four warps of a widening group + the MMA's commit
         }
         for (int b = 0; b < kSkAbufs; ++b) {
             mbar_init(aready0 + 8u * b, 4);
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8u * b, 1);
-            mbar_init(acce0 + 8u * b, 4);
+            mbar_init(acce0 + 8u * b, kSkEpiWarps);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0u;
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             const uint64_t pol_keep = policy_evict_last();
             uint32_t n_iss = 0;
             for (int64_t i = lo; i < hi; ++i, ++n_iss) {
-                const uint32_t s = n_iss % kSkStages, ph = (n_iss / kSkStages) & 1u;
+                const uint32_t s = n_iss % Cfg::STAGES, ph = (n_iss / Cfg::STAGES) & 1u;
                 if (!wait_bounded(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) break;
                 const int tile = static_cast<int>(i / p.num_kb);
                 const int kb = static_cast<int>(i % p.num_kb);
@@ -187,9 +193,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 tma_load_2d(st, &tmB, kb * 64, tile * 128, full0 + 8u * s, pol_stream);
                 tma_load_2d(st + kSkBtBytes, &tmA, kb * 64, 0, full0 + 8u * s, pol_keep);
             }
-            for (uint32_t s = 0; s < static_cast<uint32_t>(kSkStages) && s < n_iss; ++s) {
-                const uint32_t last = s + ((n_iss - 1u - s) / kSkStages) * kSkStages;
-                wait_bounded(full0 + 8u * s, (last / kSkStages) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
+            for (uint32_t s = 0; s < static_cast<uint32_t>(Cfg::STAGES) && s < n_iss; ++s) {
+                const uint32_t last = s + ((n_iss - 1u - s) / Cfg::STAGES) * Cfg::STAGES;
+                wait_bounded(full0 + 8u * s, (last / Cfg::STAGES) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
             }
         }
     } else if (warp == 1) {
@@ -209,7 +215,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     chunk_open = true;
                     first = 1;
                 }
-                const uint32_t s = n % kSkStages, ph = (n / kSkStages) & 1u;
+                const uint32_t s = n % Cfg::STAGES, ph = (n / Cfg::STAGES) & 1u;
                 const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
                 if (!wait_bounded(full0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutMma)) break;
                 if (!wait_bounded(aready0 + 8u * b, bph, abort_flag, p.err, kDevErrTimeoutMma)) break;
@@ -232,14 +238,15 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             mma_commit(done_bar);
             wait_bounded(done_bar, 0u, nullptr, p.err, kDevErrTimeoutTeardown);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= kSkWidenWarp0 && warp < kSkEpiWarp0) {
         // ---------------------------------------------------------- widen --
         const int q = warp & 3;
+        const int g = (warp - kSkWidenWarp0) >> 2;   // this warp's group: K steps n = g mod kSkGroups
         const int row = q * 32 + lane;            // row of the 128-row Bt box
         const uint32_t swz = (row >> 1) & 3;      // 64-byte swizzle of this row
-        uint32_t n = 0;
-        for (int64_t i = lo; i < hi; ++i, ++n) {
-            const uint32_t s = n % kSkStages, ph = (n / kSkStages) & 1u;
+        uint32_t n = g;
+        for (int64_t i = lo + g; i < hi; i += kSkGroups, n += kSkGroups) {
+            const uint32_t s = n % Cfg::STAGES, ph = (n / Cfg::STAGES) & 1u;
             const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
             int got = 1;
             if (lane == 0) {
@@ -250,22 +257,28 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (!got) break;
             tc_fence_after();
             const uint32_t src = base + s * Cfg::STAGE_BYTES + row * 64;
-            uint32_t w[32];
+            const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 32;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint4 v = ld_shared_v4(src + ((c ^ swz) << 4));
-                const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u;
-                const uint32_t x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;
-                w[8 * c + 0] = i8x2_to_f16x2(x0, 0x4140u);
-                w[8 * c + 1] = i8x2_to_f16x2(x0, 0x4342u);
-                w[8 * c + 2] = i8x2_to_f16x2(x1, 0x4140u);
-                w[8 * c + 3] = i8x2_to_f16x2(x1, 0x4342u);
-                w[8 * c + 4] = i8x2_to_f16x2(x2, 0x4140u);
-                w[8 * c + 5] = i8x2_to_f16x2(x2, 0x4342u);
-                w[8 * c + 6] = i8x2_to_f16x2(x3, 0x4140u);
-                w[8 * c + 7] = i8x2_to_f16x2(x3, 0x4342u);
+            for (int hf = 0; hf < 2; ++hf) {
+                // 32 int8 of the row -> 32 f16 in 16 TMEM columns
+                uint32_t w[16];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * hf + cc;
+                    const uint4 v = ld_shared_v4(src + ((c ^ swz) << 4));
+                    const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u;
+                    const uint32_t x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;
+                    w[8 * cc + 0] = i8x2_to_f16x2(x0, 0x4140u);
+                    w[8 * cc + 1] = i8x2_to_f16x2(x0, 0x4342u);
+                    w[8 * cc + 2] = i8x2_to_f16x2(x1, 0x4140u);
+                    w[8 * cc + 3] = i8x2_to_f16x2(x1, 0x4342u);
+                    w[8 * cc + 4] = i8x2_to_f16x2(x2, 0x4140u);
+                    w[8 * cc + 5] = i8x2_to_f16x2(x2, 0x4342u);
+                    w[8 * cc + 6] = i8x2_to_f16x2(x3, 0x4140u);
+                    w[8 * cc + 7] = i8x2_to_f16x2(x3, 0x4342u);
+                }
+                tmem_st_32x32b_x16(dst + hf * 16, w);
             }
-            tmem_st_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 32, w);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -274,13 +287,15 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 mbar_arrive(empty0 + 8u * s);
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= kSkEpiWarp0) {
         // ------------------------------------------------------- epilogue --
+        // Every drained chunk (at most 1024 K elements, an exact integer in
+        // fp32) is added into C at once: no running sums held in registers.
         const int q = warp & 3;
+        const int half = (warp - kSkEpiWarp0) >> 2;   // which half of the NP columns
+        const int col0 = half * Cfg::EPI_COLS;
         const int jrow = q * 32 + lane;           // TMEM lane = row of the Bt tile = column j of C
-        int32_t sum[NP];
-#pragma unroll
-        for (int c = 0; c < NP; ++c) sum[c] = 0;
+        const int rows = min(Cfg::EPI_COLS, p.m - col0);
         uint32_t chunk_iter = 0;
         for (int64_t i = lo; i < hi; ++i) {
             if (!chunk_ends(p, i, hi)) continue;
@@ -290,29 +305,24 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) break;
             tc_fence_after();
-            const uint32_t taddr = tmem_acc + buf * NP + (static_cast<uint32_t>(q * 32) << 16);
+            const uint32_t taddr = tmem_acc + buf * NP + col0 + (static_cast<uint32_t>(q * 32) << 16);
+            const int64_t j = static_cast<int64_t>(i / p.num_kb) * 128 + jrow;
+            int32_t* out = p.C + static_cast<int64_t>(col0) * p.n + j;
 #pragma unroll
-            for (int c0 = 0; c0 < NP; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(taddr + c0, v);
+            for (int c0 = 0; c0 < Cfg::EPI_COLS; c0 += 8) {
+                uint32_t v[8];
+                tmem_ld_32x32b_x8(taddr + c0, v);
                 tmem_wait_ld();
+                if (j < p.n) {
 #pragma unroll
-                for (int c = 0; c < 16; ++c) sum[c0 + c] += __float2int_rn(__uint_as_float(v[c]));
+                    for (int c = 0; c < 8; ++c)
+                        if (c0 + c < rows) atomicAdd(out + static_cast<int64_t>(c0 + c) * p.n, __float2int_rn(__uint_as_float(v[c])));
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8u * buf);
             ++chunk_iter;
-            if (segment_ends(p, i, hi)) {
-                const int64_t j = static_cast<int64_t>(i / p.num_kb) * 128 + jrow;
-                if (j < p.n) {
-#pragma unroll
-                    for (int c = 0; c < NP; ++c)
-                        if (c < p.m) atomicAdd(p.C + static_cast<int64_t>(c) * p.n + j, sum[c]);
-                }
-#pragma unroll
-                for (int c = 0; c < NP; ++c) sum[c] = 0;
-            }
         }
     }
 
