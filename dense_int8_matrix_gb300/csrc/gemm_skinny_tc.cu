@@ -7,24 +7,30 @@
 // its N side is m padded to NP in {16, 32, 64}, fp32 accumulation in TMEM,
 // drained to exact int32 every 1024 K elements as in the large kernel.
 //
-// Data path per 64-element K step, per CTA (28 warps):
-//   warp 0      TMA: the int8 Bt box (64 B x 128 rows, 64-byte swizzle) and
-//               the f16 activation box (64 x NP, 128-byte swizzle) into one
-//               stage of a 12-16-deep shared-memory ring;
-//   warps 4-19  widen, in four groups of four warps that take the K steps in
+// A pipeline stage is 256 K elements (four K steps of 64): every Bt row is
+// fetched as 256 contiguous bytes (two 128-byte TMA boxes), which a stream of
+// short row fragments cannot match (measured on GB300: 64-byte rows stream
+// at ~4.3 TB/s, 128-byte rows at ~6.5 TB/s, 256-byte rows at ~6.9 TB/s).
+//
+// Roles, per CTA (20 warps):
+//   warp 0      TMA: the int8 Bt boxes (128 rows x 256 B, 128-byte swizzle)
+//               into a 4-5-deep ring;
+//   warp 2      TMA: the f16 activation boxes (NP rows x 256 K) into a
+//               2-3-deep ring (they are re-read by every CTA and stay in L2);
+//   warps 4-11  widen, in two groups of four warps that take the stages in
 //               turn (one warp of a group per TMEM lane quarter): each lane
-//               reads its Bt row (64 int8) from shared memory, widens it to
+//               reads its Bt row (256 int8) from shared memory, widens it to
 //               f16 in registers (exact) and writes it with tcgen05.st into
-//               one of eight TMEM operand buffers.  The MMA reads its A
-//               operand from TMEM, so shared memory carries only the int8
-//               bytes (read once) and the small activation tile;
+//               one of three 128-column TMEM operand buffers.  The MMA reads
+//               its A operand from TMEM, so shared memory carries only the
+//               int8 bytes, read once;
 //   warp 1      tcgen05.mma (A from TMEM, B = activations from shared memory)
 //               into one of two TMEM accumulators;
-//   warps 20-27 drain each accumulator chunk (two warps per lane quarter,
+//   warps 12-19 drain each accumulator chunk (two warps per lane quarter,
 //               half of the NP columns each), convert it to int32 (exact) and
 //               add it into C (pre-zeroed) with coalesced integer atomics:
 //               exact and order-free.
-// Work split ("stream-K"): the (row tile, K step) iterations are numbered
+// Work split ("stream-K"): the (128-row tile, stage) iterations are numbered
 // tile-major and every CTA takes an equal contiguous range, so all SMs
 // stream the same number of Bt bytes.
 #include <cuda.h>
@@ -39,24 +45,28 @@ namespace gemm {
 
 namespace {
 
-constexpr int kSkBtBytes = 128 * 64;       // int8 Bt box per stage
-constexpr int kSkGroups = 4;               // widening groups (4 warps each)
-constexpr int kSkAbufs = 2 * kSkGroups;    // TMEM operand buffers (32 columns each)
+constexpr int kSkKbPerStage = 4;                     // K steps of 64 per stage
+constexpr int kSkBtBox = 128 * 128;                  // one 128 B x 128-row box
+constexpr int kSkBtStage = 2 * kSkBtBox;             // 256 B x 128 rows
+constexpr int kSkGroups = 2;                         // widening groups (4 warps each)
+constexpr int kSkAbufs = 3;                          // TMEM operand buffers, 128 columns each
 constexpr int kSkEpiWarps = 8;
 constexpr int kSkWidenWarp0 = 4;
 constexpr int kSkEpiWarp0 = kSkWidenWarp0 + 4 * kSkGroups;
-constexpr int kSkThreads = 32 * (kSkEpiWarp0 + kSkEpiWarps);   // 896
-constexpr int kSkChunkKb = kI8ChunkK / 64; // K steps per exact fp32 chunk
+constexpr int kSkThreads = 32 * (kSkEpiWarp0 + kSkEpiWarps);   // 640
+constexpr int kSkChunkStages = kI8ChunkK / (64 * kSkKbPerStage);  // stages per exact fp32 chunk
 
 template <int NP>
 struct SkCfg {
-    static constexpr int ACT_BYTES = NP * 128;                 // f16 activation box per stage
-    static constexpr int STAGE_BYTES = kSkBtBytes + ACT_BYTES;  // multiple of 1024
-    static constexpr int STAGES = NP >= 64 ? 12 : 16;
-    static constexpr int TMEM_COLS = 512;                      // 8 x 32 operand + 2 x NP accumulator
+    static constexpr int ACT_BOX = NP * 128;                   // f16 activation box: 64 K x NP rows
+    static constexpr int ACT_STAGE = kSkKbPerStage * ACT_BOX;
+    static constexpr int BT_STAGES = NP >= 64 ? 4 : 5;
+    static constexpr int ACT_STAGES = NP >= 64 ? 2 : 3;
+    static constexpr int TMEM_COLS = 512;                      // 3 x 128 operand + 2 x NP accumulator
     static constexpr int EPI_COLS = NP / 2;                    // columns per epilogue warp
-    static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 1024;
-    static_assert(kSkAbufs * 32 + 2 * NP <= TMEM_COLS, "TMEM budget");
+    static constexpr size_t SMEM =
+        static_cast<size_t>(BT_STAGES) * kSkBtStage + static_cast<size_t>(ACT_STAGES) * ACT_STAGE + 1024 + 1024;
+    static_assert(kSkAbufs * 128 + 2 * NP <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -64,9 +74,9 @@ struct SkParams {
     int32_t* C;
     int* err;
     int m, n;
-    int num_kb;       // K steps of 64
+    int num_sb;       // stages of 256 K per tile
     int tiles;        // ceil(n / 128)
-    int64_t iters;    // tiles * num_kb
+    int64_t iters;    // tiles * num_sb
 };
 
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -110,16 +120,29 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t biased, uint32_t sele
     return out;
 }
 
-// The iteration range of one CTA and the chunk structure inside it: a chunk
-// ends after a K step that closes 16 K steps of a tile, the tile, or the range.
+__device__ __forceinline__ void widen16(const uint4 v, uint32_t* w) {
+    const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u;
+    const uint32_t x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;
+    w[0] = i8x2_to_f16x2(x0, 0x4140u);
+    w[1] = i8x2_to_f16x2(x0, 0x4342u);
+    w[2] = i8x2_to_f16x2(x1, 0x4140u);
+    w[3] = i8x2_to_f16x2(x1, 0x4342u);
+    w[4] = i8x2_to_f16x2(x2, 0x4140u);
+    w[5] = i8x2_to_f16x2(x2, 0x4342u);
+    w[6] = i8x2_to_f16x2(x3, 0x4140u);
+    w[7] = i8x2_to_f16x2(x3, 0x4342u);
+}
+
 __device__ __forceinline__ void cta_range(const SkParams& p, int64_t& lo, int64_t& hi) {
     lo = p.iters * blockIdx.x / gridDim.x;
     hi = p.iters * (blockIdx.x + 1) / gridDim.x;
 }
 
+// A chunk ends after a stage that closes 1024 K elements of a tile, the
+// tile, or the CTA's range.
 __device__ __forceinline__ bool chunk_ends(const SkParams& p, int64_t i, int64_t hi) {
-    const int kb = static_cast<int>(i % p.num_kb);
-    return (i + 1 == hi) || (kb + 1 == p.num_kb) || ((kb + 1) % kSkChunkKb == 0);
+    const int sb = static_cast<int>(i % p.num_sb);
+    return (i + 1 == hi) || (sb + 1 == p.num_sb) || ((sb + 1) % kSkChunkStages == 0);
 }
 
 template <int NP>
@@ -130,25 +153,34 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* ctrl = smem_raw + (base - raw) + Cfg::STAGES * Cfg::STAGE_BYTES;
+    const uint32_t sBt = base;
+    const uint32_t sAct = base + Cfg::BT_STAGES * kSkBtStage;
+    uint8_t* ctrl = smem_raw + (base - raw) + Cfg::BT_STAGES * kSkBtStage + Cfg::ACT_STAGES * Cfg::ACT_STAGE;
     const uint32_t bar0 = smem_u32(ctrl);
-    const uint32_t full0 = bar0;                          // [Cfg::STAGES]
-    const uint32_t empty0 = full0 + 8u * Cfg::STAGES;       // [Cfg::STAGES]
-    const uint32_t aready0 = empty0 + 8u * Cfg::STAGES;     // [kSkAbufs]
-    const uint32_t afree0 = aready0 + 8u * kSkAbufs;      // [kSkAbufs]
-    const uint32_t accf0 = afree0 + 8u * kSkAbufs;        // [2]
-    const uint32_t acce0 = accf0 + 16u;                   // [2]
+    const uint32_t fullB0 = bar0;                              // [BT_STAGES]
+    const uint32_t emptyB0 = fullB0 + 8u * Cfg::BT_STAGES;     // [BT_STAGES]
+    const uint32_t fullA0 = emptyB0 + 8u * Cfg::BT_STAGES;     // [ACT_STAGES]
+    const uint32_t emptyA0 = fullA0 + 8u * Cfg::ACT_STAGES;    // [ACT_STAGES]
+    const uint32_t aready0 = emptyA0 + 8u * Cfg::ACT_STAGES;   // [kSkAbufs]
+    const uint32_t afree0 = aready0 + 8u * kSkAbufs;           // [kSkAbufs]
+    const uint32_t accf0 = afree0 + 8u * kSkAbufs;             // [2]
+    const uint32_t acce0 = accf0 + 16u;                        // [2]
     const uint32_t done_bar = acce0 + 16u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * Cfg::STAGES + 2 * kSkAbufs + 5));
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * Cfg::BT_STAGES + 2 * Cfg::ACT_STAGES + 2 * kSkAbufs + 5));
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < Cfg::STAGES; ++s) {
-            mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, 4 + 1);   // the four warps of a widening group + the MMA's commit
+        for (int s = 0; s < Cfg::BT_STAGES; ++s) {
+            mbar_init(fullB0 + 8u * s, 1);
+            mbar_init(emptyB0 + 8u * s, 4);   // the four warps of the widening group
+        }
+        for (int s = 0; s < Cfg::ACT_STAGES; ++s) {
+            mbar_init(fullA0 + 8u * s, 1);
+            mbar_init(emptyA0 + 8u * s, 1);   // the MMA's commit
         }
         for (int b = 0; b < kSkAbufs; ++b) {
             mbar_init(aready0 + 8u * b, 4);
@@ -170,32 +202,51 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tmem_acc = tmem_base + kSkAbufs * 32;   // two accumulators of NP columns
+    const uint32_t tmem_acc = tmem_base + kSkAbufs * 128;   // two accumulators of NP columns
 
     int64_t lo, hi;
     cta_range(p, lo, hi);
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA --
+        // ------------------------------------------------------- TMA: Bt --
         if (lane == 0) {
             tma_prefetch_desc(&tmB);
-            tma_prefetch_desc(&tmA);
-            const uint64_t pol_stream = policy_evict_first();
-            const uint64_t pol_keep = policy_evict_last();
+            const uint64_t pol = policy_evict_first();
             uint32_t n_iss = 0;
             for (int64_t i = lo; i < hi; ++i, ++n_iss) {
-                const uint32_t s = n_iss % Cfg::STAGES, ph = (n_iss / Cfg::STAGES) & 1u;
-                if (!wait_bounded(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) break;
-                const int tile = static_cast<int>(i / p.num_kb);
-                const int kb = static_cast<int>(i % p.num_kb);
-                const uint32_t st = base + s * Cfg::STAGE_BYTES;
-                mbar_arrive_expect_tx(full0 + 8u * s, Cfg::STAGE_BYTES);
-                tma_load_2d(st, &tmB, kb * 64, tile * 128, full0 + 8u * s, pol_stream);
-                tma_load_2d(st + kSkBtBytes, &tmA, kb * 64, 0, full0 + 8u * s, pol_keep);
+                const uint32_t s = n_iss % Cfg::BT_STAGES, ph = (n_iss / Cfg::BT_STAGES) & 1u;
+                if (!wait_bounded(emptyB0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) break;
+                const int tile = static_cast<int>(i / p.num_sb);
+                const int x = static_cast<int>(i % p.num_sb) * 256;
+                const uint32_t dst = sBt + s * kSkBtStage;
+                mbar_arrive_expect_tx(fullB0 + 8u * s, kSkBtStage);
+                tma_load_2d(dst, &tmB, x, tile * 128, fullB0 + 8u * s, pol);
+                tma_load_2d(dst + kSkBtBox, &tmB, x + 128, tile * 128, fullB0 + 8u * s, pol);
             }
-            for (uint32_t s = 0; s < static_cast<uint32_t>(Cfg::STAGES) && s < n_iss; ++s) {
-                const uint32_t last = s + ((n_iss - 1u - s) / Cfg::STAGES) * Cfg::STAGES;
-                wait_bounded(full0 + 8u * s, (last / Cfg::STAGES) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
+            for (uint32_t s = 0; s < static_cast<uint32_t>(Cfg::BT_STAGES) && s < n_iss; ++s) {
+                const uint32_t last = s + ((n_iss - 1u - s) / Cfg::BT_STAGES) * Cfg::BT_STAGES;
+                wait_bounded(fullB0 + 8u * s, (last / Cfg::BT_STAGES) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------- TMA: activations --
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            const uint64_t pol = policy_evict_last();
+            uint32_t n_iss = 0;
+            for (int64_t i = lo; i < hi; ++i, ++n_iss) {
+                const uint32_t s = n_iss % Cfg::ACT_STAGES, ph = (n_iss / Cfg::ACT_STAGES) & 1u;
+                if (!wait_bounded(emptyA0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) break;
+                const int kb0 = static_cast<int>(i % p.num_sb) * kSkKbPerStage;
+                const uint32_t dst = sAct + s * Cfg::ACT_STAGE;
+                mbar_arrive_expect_tx(fullA0 + 8u * s, Cfg::ACT_STAGE);
+#pragma unroll
+                for (int j = 0; j < kSkKbPerStage; ++j)
+                    tma_load_2d(dst + j * Cfg::ACT_BOX, &tmA, (kb0 + j) * 64, 0, fullA0 + 8u * s, pol);
+            }
+            for (uint32_t s = 0; s < static_cast<uint32_t>(Cfg::ACT_STAGES) && s < n_iss; ++s) {
+                const uint32_t last = s + ((n_iss - 1u - s) / Cfg::ACT_STAGES) * Cfg::ACT_STAGES;
+                wait_bounded(fullA0 + 8u * s, (last / Cfg::ACT_STAGES) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
             }
         }
     } else if (warp == 1) {
@@ -203,11 +254,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(0u, 128, NP);
             uint32_t n = 0, chunk_iter = 0;
-            bool ok = true;
             bool chunk_open = false;
             uint32_t d_tmem = tmem_acc;
             uint32_t first = 1;
-            for (int64_t i = lo; ok && i < hi; ++i, ++n) {
+            for (int64_t i = lo; i < hi; ++i, ++n) {
                 if (!chunk_open) {
                     const uint32_t buf = chunk_iter & 1u, aph = (chunk_iter >> 1) & 1u;
                     if (!wait_bounded(acce0 + 8u * buf, aph ^ 1u, abort_flag, p.err, kDevErrTimeoutMma)) break;
@@ -215,20 +265,25 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     chunk_open = true;
                     first = 1;
                 }
-                const uint32_t s = n % Cfg::STAGES, ph = (n / Cfg::STAGES) & 1u;
+                const uint32_t sa = n % Cfg::ACT_STAGES, pha = (n / Cfg::ACT_STAGES) & 1u;
                 const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
-                if (!wait_bounded(full0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutMma)) break;
+                if (!wait_bounded(fullA0 + 8u * sa, pha, abort_flag, p.err, kDevErrTimeoutMma)) break;
                 if (!wait_bounded(aready0 + 8u * b, bph, abort_flag, p.err, kDevErrTimeoutMma)) break;
                 tc_fence_after();
-                const uint64_t bdesc = smem_desc_sw128_kmajor(base + s * Cfg::STAGE_BYTES + kSkBtBytes);
-                const uint32_t a_tmem = tmem_base + b * 32;
+                const uint32_t a_tmem = tmem_base + b * 128;
+                const uint32_t act = sAct + sa * Cfg::ACT_STAGE;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc + 2u * kk, idesc, (first == 0 || kk > 0) ? 1u : 0u);
+                for (int j = 0; j < kSkKbPerStage; ++j) {
+                    const uint64_t bdesc = smem_desc_sw128_kmajor(act + j * Cfg::ACT_BOX);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + 2u * kk, idesc,
+                                   (first == 0 || j > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 first = 0;
                 mma_commit(afree0 + 8u * b);
-                mma_commit(empty0 + 8u * s);
+                mma_commit(emptyA0 + 8u * sa);
                 if (chunk_ends(p, i, hi)) {
                     mma_commit(accf0 + 8u * (chunk_iter & 1u));
                     ++chunk_iter;
@@ -241,51 +296,43 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     } else if (warp >= kSkWidenWarp0 && warp < kSkEpiWarp0) {
         // ---------------------------------------------------------- widen --
         const int q = warp & 3;
-        const int g = (warp - kSkWidenWarp0) >> 2;   // this warp's group: K steps n = g mod kSkGroups
-        const int row = q * 32 + lane;            // row of the 128-row Bt box
-        const uint32_t swz = (row >> 1) & 3;      // 64-byte swizzle of this row
+        const int g = (warp - kSkWidenWarp0) >> 2;   // this warp's group: stages n = g mod kSkGroups
+        const int row = q * 32 + lane;                // row of the 128-row Bt box
+        const uint32_t swz = row & 7;                 // 128-byte swizzle of this row
         uint32_t n = g;
         for (int64_t i = lo + g; i < hi; i += kSkGroups, n += kSkGroups) {
-            const uint32_t s = n % Cfg::STAGES, ph = (n / Cfg::STAGES) & 1u;
+            const uint32_t s = n % Cfg::BT_STAGES, ph = (n / Cfg::BT_STAGES) & 1u;
             const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
             int got = 1;
             if (lane == 0) {
-                got = wait_bounded(full0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutEpilogue) &&
+                got = wait_bounded(fullB0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutEpilogue) &&
                       wait_bounded(afree0 + 8u * b, bph ^ 1u, abort_flag, p.err, kDevErrTimeoutEpilogue);
             }
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) break;
             tc_fence_after();
-            const uint32_t src = base + s * Cfg::STAGE_BYTES + row * 64;
-            const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 32;
+            // the row's 256 bytes: box 0 holds K 0..127, box 1 K 128..255
+            uint4 v[16];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                // 32 int8 of the row -> 32 f16 in 16 TMEM columns
+            for (int c = 0; c < 16; ++c) {
+                const uint32_t src = sBt + s * kSkBtStage + (c >> 3) * kSkBtBox + row * 128;
+                v[c] = ld_shared_v4(src + (((c & 7) ^ swz) << 4));
+            }
+            // the bytes are in registers: the stage can be refilled
+            __syncwarp();
+            if (lane == 0) mbar_arrive(emptyB0 + 8u * s);
+            const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 128;
+#pragma unroll
+            for (int hf = 0; hf < 8; ++hf) {
                 uint32_t w[16];
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = 2 * hf + cc;
-                    const uint4 v = ld_shared_v4(src + ((c ^ swz) << 4));
-                    const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u;
-                    const uint32_t x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;
-                    w[8 * cc + 0] = i8x2_to_f16x2(x0, 0x4140u);
-                    w[8 * cc + 1] = i8x2_to_f16x2(x0, 0x4342u);
-                    w[8 * cc + 2] = i8x2_to_f16x2(x1, 0x4140u);
-                    w[8 * cc + 3] = i8x2_to_f16x2(x1, 0x4342u);
-                    w[8 * cc + 4] = i8x2_to_f16x2(x2, 0x4140u);
-                    w[8 * cc + 5] = i8x2_to_f16x2(x2, 0x4342u);
-                    w[8 * cc + 6] = i8x2_to_f16x2(x3, 0x4140u);
-                    w[8 * cc + 7] = i8x2_to_f16x2(x3, 0x4342u);
-                }
+                widen16(v[2 * hf], w);
+                widen16(v[2 * hf + 1], w + 8);
                 tmem_st_32x32b_x16(dst + hf * 16, w);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(aready0 + 8u * b);
-                mbar_arrive(empty0 + 8u * s);
-            }
+            if (lane == 0) mbar_arrive(aready0 + 8u * b);
         }
     } else if (warp >= kSkEpiWarp0) {
         // ------------------------------------------------------- epilogue --
@@ -306,7 +353,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (!got) break;
             tc_fence_after();
             const uint32_t taddr = tmem_acc + buf * NP + col0 + (static_cast<uint32_t>(q * 32) << 16);
-            const int64_t j = static_cast<int64_t>(i / p.num_kb) * 128 + jrow;
+            const int64_t j = static_cast<int64_t>(i / p.num_sb) * 128 + jrow;
             int32_t* out = p.C + static_cast<int64_t>(col0) * p.n + j;
 #pragma unroll
             for (int c0 = 0; c0 < Cfg::EPI_COLS; c0 += 8) {
@@ -316,7 +363,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 if (j < p.n) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        if (c0 + c < rows) atomicAdd(out + static_cast<int64_t>(c0 + c) * p.n, __float2int_rn(__uint_as_float(v[c])));
+                        if (c0 + c < rows)
+                            atomicAdd(out + static_cast<int64_t>(c0 + c) * p.n, __float2int_rn(__uint_as_float(v[c])));
                 }
             }
             tc_fence_before();
@@ -344,16 +392,19 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     if (!enc) return cudaErrorInvalidValue;
     CUtensorMap mB, mA;
     {
+        // int8 Bt: 128-byte x 128-row boxes, 128-byte swizzle; K and rows
+        // beyond the matrix read as zero
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(n)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
-        cuuint32_t box[2] = {64u, 128u};
+        cuuint32_t box[2] = {128u, 128u};
         cuuint32_t estr[2] = {1u, 1u};
         if (enc(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(Bt), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     {
+        // f16 activations: 64 K x NP rows per box (rows >= m read as zero)
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2u};
         cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(NP)};
@@ -368,9 +419,9 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     p.err = err;
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
-    p.num_kb = static_cast<int>((k + 63) / 64);
+    p.num_sb = static_cast<int>((k + 255) / 256);
     p.tiles = static_cast<int>((n + 127) / 128);
-    p.iters = static_cast<int64_t>(p.tiles) * p.num_kb;
+    p.iters = static_cast<int64_t>(p.tiles) * p.num_sb;
     int64_t grid = num_sms;
     if (grid > p.iters) grid = p.iters;
     auto kern = skinny_tc_kernel<NP>;
