@@ -14,9 +14,9 @@
 //
 // Roles, per CTA (20 warps):
 //   warp 0      TMA: the int8 Bt boxes (128 rows x 256 B, 128-byte swizzle)
-//               into a 4-5-deep ring;
+//               into a 3-5-deep ring;
 //   warp 2      TMA: the f16 activation boxes (NP rows x 256 K) into a
-//               2-3-deep ring (they are re-read by every CTA and stay in L2);
+//               3-6-deep ring (they are re-read by every CTA and stay in L2);
 //   warps 4-11  widen, in two groups of four warps that take the stages in
 //               turn (one warp of a group per TMEM lane quarter): each lane
 //               reads its Bt row (256 int8) from shared memory, widens it to
@@ -60,8 +60,11 @@ template <int NP>
 struct SkCfg {
     static constexpr int ACT_BOX = NP * 128;                   // f16 activation box: 64 K x NP rows
     static constexpr int ACT_STAGE = kSkKbPerStage * ACT_BOX;
-    static constexpr int BT_STAGES = NP >= 64 ? 4 : 5;
-    static constexpr int ACT_STAGES = NP >= 64 ? 2 : 3;
+    // The activation ring must cover the MMA-to-refill latency (an L2 round
+    // trip after the MMA two or more stages back completes); the Bt ring the
+    // HBM latency.
+    static constexpr int BT_STAGES = NP >= 64 ? 3 : (NP >= 32 ? 4 : 5);
+    static constexpr int ACT_STAGES = NP >= 64 ? 3 : (NP >= 32 ? 4 : 6);
     static constexpr int TMEM_COLS = 512;                      // 3 x 128 operand + 2 x NP accumulator
     static constexpr int EPI_COLS = NP / 2;                    // columns per epilogue warp
     static constexpr size_t SMEM =
