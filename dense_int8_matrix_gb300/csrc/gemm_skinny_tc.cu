@@ -141,11 +141,29 @@ __device__ __forceinline__ void cta_range(const SkParams& p, int64_t& lo, int64_
     hi = p.iters * (blockIdx.x + 1) / gridDim.x;
 }
 
+// Position of an iteration: its 128-row tile and its stage within the tile,
+// advanced incrementally (no division inside the loops).
+struct Cursor {
+    int tile, sb;
+    __device__ __forceinline__ void advance(int num_sb) {
+        if (++sb == num_sb) {
+            sb = 0;
+            ++tile;
+        }
+    }
+};
+
+__device__ __forceinline__ Cursor cursor_at(const SkParams& p, int64_t i) {
+    Cursor c;
+    c.tile = static_cast<int>(i / p.num_sb);
+    c.sb = static_cast<int>(i - static_cast<int64_t>(c.tile) * p.num_sb);
+    return c;
+}
+
 // A chunk ends after a stage that closes 1024 K elements of a tile, the
-// tile, or the CTA's range.
-__device__ __forceinline__ bool chunk_ends(const SkParams& p, int64_t i, int64_t hi) {
-    const int sb = static_cast<int>(i % p.num_sb);
-    return (i + 1 == hi) || (sb + 1 == p.num_sb) || ((sb + 1) % kSkChunkStages == 0);
+// tile, or the CTA's range (`last`).
+__device__ __forceinline__ bool chunk_ends(const SkParams& p, const Cursor& c, bool last) {
+    return last || (c.sb + 1 == p.num_sb) || ((c.sb + 1) % kSkChunkStages == 0);
 }
 
 template <int NP>
@@ -216,11 +234,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             tma_prefetch_desc(&tmB);
             const uint64_t pol = policy_evict_first();
             uint32_t n_iss = 0;
-            for (int64_t i = lo; i < hi; ++i, ++n_iss) {
+            Cursor c = cursor_at(p, lo);
+            for (int64_t i = lo; i < hi; ++i, ++n_iss, c.advance(p.num_sb)) {
                 const uint32_t s = n_iss % Cfg::BT_STAGES, ph = (n_iss / Cfg::BT_STAGES) & 1u;
                 if (!wait_bounded(emptyB0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) break;
-                const int tile = static_cast<int>(i / p.num_sb);
-                const int x = static_cast<int>(i % p.num_sb) * 256;
+                const int tile = c.tile;
+                const int x = c.sb * 256;
                 const uint32_t dst = sBt + s * kSkBtStage;
                 mbar_arrive_expect_tx(fullB0 + 8u * s, kSkBtStage);
                 tma_load_2d(dst, &tmB, x, tile * 128, fullB0 + 8u * s, pol);
@@ -237,10 +256,11 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             tma_prefetch_desc(&tmA);
             const uint64_t pol = policy_evict_last();
             uint32_t n_iss = 0;
-            for (int64_t i = lo; i < hi; ++i, ++n_iss) {
+            Cursor c = cursor_at(p, lo);
+            for (int64_t i = lo; i < hi; ++i, ++n_iss, c.advance(p.num_sb)) {
                 const uint32_t s = n_iss % Cfg::ACT_STAGES, ph = (n_iss / Cfg::ACT_STAGES) & 1u;
                 if (!wait_bounded(emptyA0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) break;
-                const int kb0 = static_cast<int>(i % p.num_sb) * kSkKbPerStage;
+                const int kb0 = c.sb * kSkKbPerStage;
                 const uint32_t dst = sAct + s * Cfg::ACT_STAGE;
                 mbar_arrive_expect_tx(fullA0 + 8u * s, Cfg::ACT_STAGE);
 #pragma unroll
@@ -260,7 +280,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             bool chunk_open = false;
             uint32_t d_tmem = tmem_acc;
             uint32_t first = 1;
-            for (int64_t i = lo; i < hi; ++i, ++n) {
+            Cursor c = cursor_at(p, lo);
+            for (int64_t i = lo; i < hi; ++i, ++n, c.advance(p.num_sb)) {
                 if (!chunk_open) {
                     const uint32_t buf = chunk_iter & 1u, aph = (chunk_iter >> 1) & 1u;
                     if (!wait_bounded(acce0 + 8u * buf, aph ^ 1u, abort_flag, p.err, kDevErrTimeoutMma)) break;
@@ -287,7 +308,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 first = 0;
                 mma_commit(afree0 + 8u * b);
                 mma_commit(emptyA0 + 8u * sa);
-                if (chunk_ends(p, i, hi)) {
+                if (chunk_ends(p, c, i + 1 == hi)) {
                     mma_commit(accf0 + 8u * (chunk_iter & 1u));
                     ++chunk_iter;
                     chunk_open = false;
@@ -347,8 +368,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const int jrow = q * 32 + lane;           // TMEM lane = row of the Bt tile = column j of C
         const int rows = min(Cfg::EPI_COLS, p.m - col0);
         uint32_t chunk_iter = 0;
-        for (int64_t i = lo; i < hi; ++i) {
-            if (!chunk_ends(p, i, hi)) continue;
+        Cursor c = cursor_at(p, lo);
+        for (int64_t i = lo; i < hi; ++i, c.advance(p.num_sb)) {
+            if (!chunk_ends(p, c, i + 1 == hi)) continue;
             const uint32_t buf = chunk_iter & 1u, aph = (chunk_iter >> 1) & 1u;
             int got = 1;
             if (lane == 0) got = wait_bounded(accf0 + 8u * buf, aph, abort_flag, p.err, kDevErrTimeoutEpilogue);
@@ -356,7 +378,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (!got) break;
             tc_fence_after();
             const uint32_t taddr = tmem_acc + buf * NP + col0 + (static_cast<uint32_t>(q * 32) << 16);
-            const int64_t j = static_cast<int64_t>(i / p.num_sb) * 128 + jrow;
+            const int64_t j = static_cast<int64_t>(c.tile) * 128 + jrow;
             int32_t* out = p.C + static_cast<int64_t>(col0) * p.n + j;
 #pragma unroll
             for (int c0 = 0; c0 < Cfg::EPI_COLS; c0 += 8) {
