@@ -12,24 +12,24 @@
 // short row fragments cannot match (measured on GB300: 64-byte rows stream
 // at ~4.3 TB/s, 128-byte rows at ~6.5 TB/s, 256-byte rows at ~6.9 TB/s).
 //
-// Roles, per CTA (20 warps):
+// Roles, per CTA (20 warps; warp 1 only owns the TMEM allocation):
 //   warp 0      TMA: the int8 Bt boxes (128 rows x 256 B, 128-byte swizzle)
 //               into a 3-5-deep ring;
 //   warp 2      TMA: the f16 activation boxes (NP rows x 256 K) into a
 //               3-6-deep ring (they are re-read by every CTA and stay in L2);
-//   warps 4-11  widen, in two groups of four warps that take the stages in
-//               turn (one warp of a group per TMEM lane quarter): each lane
-//               reads its Bt row (256 int8) from shared memory, widens it to
-//               f16 in registers (exact) and writes it with tcgen05.st into
-//               one of three 128-column TMEM operand buffers.  The MMA reads
-//               its A operand from TMEM, so shared memory carries only the
-//               int8 bytes, read once;
-//   warp 1      tcgen05.mma (A from TMEM, B = activations from shared memory)
-//               into one of two TMEM accumulators;
+//   warps 4-11  two groups of four warps that take the stages in turn (one
+//               warp of a group per TMEM lane quarter): each lane reads its
+//               Bt row (256 int8) from shared memory, widens it to f16 in
+//               registers (exact) and writes it with tcgen05.st into one of
+//               three 128-column TMEM operand buffers; then one thread of the
+//               group issues the stage's tcgen05.mma (A from TMEM, B =
+//               activations from shared memory).  Two issuers keep the tensor
+//               pipe fed while each waits for its next stage.  Shared memory
+//               carries only the int8 bytes, read once;
 //   warps 12-19 drain each accumulator chunk (two warps per lane quarter,
-//               half of the NP columns each), convert it to int32 (exact) and
-//               add it into C (pre-zeroed) with coalesced integer atomics:
-//               exact and order-free.
+//               half of the NP columns each), convert it to int32 (exact),
+//               add it into C (pre-zeroed) with coalesced integer atomics
+//               (exact and order-free) and zero the accumulator again.
 // Work split ("stream-K"): the (128-row tile, stage) iterations are numbered
 // tile-major and every CTA takes an equal contiguous range, so all SMs
 // stream the same number of Bt bytes.
@@ -95,6 +95,12 @@ __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -208,10 +214,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             mbar_init(afree0 + 8u * b, 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf0 + 8u * b, 1);
+            mbar_init(accf0 + 8u * b, kSkGroups);   // one arrival per widening group
             mbar_init(acce0 + 8u * b, kSkEpiWarps);
         }
-        mbar_init(done_bar, 1);
+        mbar_init(done_bar, kSkGroups);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -272,112 +278,148 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 wait_bounded(fullA0 + 8u * s, (last / Cfg::ACT_STAGES) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA --
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(0u, 128, NP);
-            uint32_t n = 0, chunk_iter = 0;
-            bool chunk_open = false;
-            uint32_t d_tmem = tmem_acc;
-            uint32_t first = 1;
-            Cursor c = cursor_at(p, lo);
-            for (int64_t i = lo; i < hi; ++i, ++n, c.advance(p.num_sb)) {
-                if (!chunk_open) {
-                    const uint32_t buf = chunk_iter & 1u, aph = (chunk_iter >> 1) & 1u;
-                    if (!wait_bounded(acce0 + 8u * buf, aph ^ 1u, abort_flag, p.err, kDevErrTimeoutMma)) break;
-                    d_tmem = tmem_acc + buf * NP;
-                    chunk_open = true;
-                    first = 1;
-                }
-                const uint32_t sa = n % Cfg::ACT_STAGES, pha = (n / Cfg::ACT_STAGES) & 1u;
-                const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
-                if (!wait_bounded(fullA0 + 8u * sa, pha, abort_flag, p.err, kDevErrTimeoutMma)) break;
-                if (!wait_bounded(aready0 + 8u * b, bph, abort_flag, p.err, kDevErrTimeoutMma)) break;
-                tc_fence_after();
-                const uint32_t a_tmem = tmem_base + b * 128;
-                const uint32_t act = sAct + sa * Cfg::ACT_STAGE;
-#pragma unroll
-                for (int j = 0; j < kSkKbPerStage; ++j) {
-                    const uint64_t bdesc = smem_desc_sw128_kmajor(act + j * Cfg::ACT_BOX);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + 2u * kk, idesc,
-                                   (first == 0 || j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
-                first = 0;
-                mma_commit(afree0 + 8u * b);
-                mma_commit(emptyA0 + 8u * sa);
-                if (chunk_ends(p, c, i + 1 == hi)) {
-                    mma_commit(accf0 + 8u * (chunk_iter & 1u));
-                    ++chunk_iter;
-                    chunk_open = false;
-                }
-            }
-            mma_commit(done_bar);
-            wait_bounded(done_bar, 0u, nullptr, p.err, kDevErrTimeoutTeardown);
-        }
     } else if (warp >= kSkWidenWarp0 && warp < kSkEpiWarp0) {
-        // ---------------------------------------------------------- widen --
+        // ------------------------------------------------- widen + MMA --
+        // Group g takes stages n = g, g + 2, ...  For each: widen the Bt rows
+        // into a TMEM operand buffer, sync the group, and one thread issues
+        // the stage's 16 MMAs into the chunk's accumulator (both groups add
+        // into the same, pre-zeroed accumulator: integer sums are order-free).
+        // At every chunk end each group arrives once on accf: by commit if it
+        // issued MMAs in the chunk, by a plain arrival otherwise.
         const int q = warp & 3;
-        const int g = (warp - kSkWidenWarp0) >> 2;   // this warp's group: stages n = g mod kSkGroups
+        const int g = (warp - kSkWidenWarp0) >> 2;
+        const bool issuer = (q == 0) && (lane == 0);
         const int row = q * 32 + lane;                // row of the 128-row Bt box
         const uint32_t swz = row & 7;                 // 128-byte swizzle of this row
-        uint32_t n = g;
-        for (int64_t i = lo + g; i < hi; i += kSkGroups, n += kSkGroups) {
-            const uint32_t s = n % Cfg::BT_STAGES, ph = (n / Cfg::BT_STAGES) & 1u;
-            const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
-            int got = 1;
-            if (lane == 0) {
-                got = wait_bounded(fullB0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutEpilogue) &&
-                      wait_bounded(afree0 + 8u * b, bph ^ 1u, abort_flag, p.err, kDevErrTimeoutEpilogue);
-            }
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) break;
-            tc_fence_after();
-            // the row's 256 bytes: box 0 holds K 0..127, box 1 K 128..255
-            uint4 v[16];
+        constexpr uint32_t idesc = idesc_f16(0u, 128, NP);
+        bool ok = true;
+        uint32_t ch = 0;            // chunk index of the current stage
+        bool issued_in_chunk = false;
+        bool acc_ready = false;     // this group has waited for the chunk's accumulator
+        Cursor c = cursor_at(p, lo);
+        uint32_t n = 0;
+        for (int64_t i = lo; i < hi; ++i, ++n, c.advance(p.num_sb)) {
+            const bool mine = (n & 1u) == static_cast<uint32_t>(g);
+            const uint32_t buf = ch & 1u;
+            if (mine && ok) {
+                const uint32_t s = n % Cfg::BT_STAGES, ph = (n / Cfg::BT_STAGES) & 1u;
+                const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
+                int got = 1;
+                if (lane == 0) {
+                    got = wait_bounded(fullB0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutEpilogue) &&
+                          wait_bounded(afree0 + 8u * b, bph ^ 1u, abort_flag, p.err, kDevErrTimeoutEpilogue);
+                }
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                } else {
+                    tc_fence_after();
+                    // the row's 256 bytes: box 0 holds K 0..127, box 1 K 128..255
+                    uint4 v[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint32_t src = sBt + s * kSkBtStage + (c >> 3) * kSkBtBox + row * 128;
-                v[c] = ld_shared_v4(src + (((c & 7) ^ swz) << 4));
-            }
-            // the bytes are in registers: the stage can be refilled
-            __syncwarp();
-            if (lane == 0) mbar_arrive(emptyB0 + 8u * s);
-            const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 128;
+                    for (int cc = 0; cc < 16; ++cc) {
+                        const uint32_t src = sBt + s * kSkBtStage + (cc >> 3) * kSkBtBox + row * 128;
+                        v[cc] = ld_shared_v4(src + (((cc & 7) ^ swz) << 4));
+                    }
+                    // the bytes are in registers: the stage can be refilled
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(emptyB0 + 8u * s);
+                    const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 128;
 #pragma unroll
-            for (int hf = 0; hf < 8; ++hf) {
-                uint32_t w[16];
-                widen16(v[2 * hf], w);
-                widen16(v[2 * hf + 1], w + 8);
-                tmem_st_32x32b_x16(dst + hf * 16, w);
+                    for (int hf = 0; hf < 8; ++hf) {
+                        uint32_t w[16];
+                        widen16(v[2 * hf], w);
+                        widen16(v[2 * hf + 1], w + 8);
+                        tmem_st_32x32b_x16(dst + hf * 16, w);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    // the four warps of the group have written the buffer
+                    asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
+                    if (issuer) {
+                        const uint32_t sa = n % Cfg::ACT_STAGES, pha = (n / Cfg::ACT_STAGES) & 1u;
+                        bool ready = wait_bounded(fullA0 + 8u * sa, pha, abort_flag, p.err, kDevErrTimeoutMma);
+                        if (ready && !acc_ready)
+                            ready = wait_bounded(acce0 + 8u * buf, (ch >> 1) & 1u, abort_flag, p.err,
+                                                 kDevErrTimeoutMma);
+                        if (ready) {
+                            acc_ready = true;
+                            tc_fence_after();
+                            const uint32_t d_tmem = tmem_acc + buf * NP;
+                            const uint32_t a_tmem = tmem_base + b * 128;
+                            const uint32_t act = sAct + sa * Cfg::ACT_STAGE;
+#pragma unroll
+                            for (int j = 0; j < kSkKbPerStage; ++j) {
+                                const uint64_t bdesc = smem_desc_sw128_kmajor(act + j * Cfg::ACT_BOX);
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + 2u * kk, idesc, 1u);
+                            }
+                            mma_commit(afree0 + 8u * b);
+                            mma_commit(emptyA0 + 8u * sa);
+                            issued_in_chunk = true;
+                        } else {
+                            ok = false;
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(aready0 + 8u * b);
+            if (chunk_ends(p, c, i + 1 == hi)) {
+                if (issuer && ok) {
+                    if (issued_in_chunk)
+                        mma_commit(accf0 + 8u * buf);
+                    else
+                        mbar_arrive(accf0 + 8u * buf);
+                }
+                issued_in_chunk = false;
+                acc_ready = false;
+                ++ch;
+            }
+        }
+        // Teardown: every MMA this group issued must complete before TMEM is freed.
+        if (issuer) {
+            mma_commit(done_bar);
+            wait_bounded(done_bar, 0u, nullptr, p.err, kDevErrTimeoutTeardown);
         }
     } else if (warp >= kSkEpiWarp0) {
         // ------------------------------------------------------- epilogue --
         // Every drained chunk (at most 1024 K elements, an exact integer in
-        // fp32) is added into C at once: no running sums held in registers.
+        // fp32) is added into C at once, and the accumulator is zeroed for its
+        // next chunk (the MMAs only ever accumulate).
         const int q = warp & 3;
         const int half = (warp - kSkEpiWarp0) >> 2;   // which half of the NP columns
         const int col0 = half * Cfg::EPI_COLS;
         const int jrow = q * 32 + lane;           // TMEM lane = row of the Bt tile = column j of C
         const int rows = min(Cfg::EPI_COLS, p.m - col0);
-        uint32_t chunk_iter = 0;
+        const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+        uint32_t zero[16];
+#pragma unroll
+        for (int z = 0; z < 16; ++z) zero[z] = 0u;
+        // both accumulators start at zero
+#pragma unroll
+        for (int bz = 0; bz < 2; ++bz)
+#pragma unroll
+            for (int c0 = 0; c0 < Cfg::EPI_COLS; c0 += 8)
+                tmem_st_32x32b_x8(tmem_acc + bz * NP + col0 + c0 + lanes, zero);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(acce0);
+            mbar_arrive(acce0 + 8u);
+        }
+        uint32_t ch = 0;
         Cursor c = cursor_at(p, lo);
         for (int64_t i = lo; i < hi; ++i, c.advance(p.num_sb)) {
             if (!chunk_ends(p, c, i + 1 == hi)) continue;
-            const uint32_t buf = chunk_iter & 1u, aph = (chunk_iter >> 1) & 1u;
+            const uint32_t buf = ch & 1u, aph = (ch >> 1) & 1u;
             int got = 1;
             if (lane == 0) got = wait_bounded(accf0 + 8u * buf, aph, abort_flag, p.err, kDevErrTimeoutEpilogue);
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) break;
             tc_fence_after();
-            const uint32_t taddr = tmem_acc + buf * NP + col0 + (static_cast<uint32_t>(q * 32) << 16);
+            const uint32_t taddr = tmem_acc + buf * NP + col0 + lanes;
             const int64_t j = static_cast<int64_t>(c.tile) * 128 + jrow;
             int32_t* out = p.C + static_cast<int64_t>(col0) * p.n + j;
 #pragma unroll
@@ -385,17 +427,19 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 uint32_t v[8];
                 tmem_ld_32x32b_x8(taddr + c0, v);
                 tmem_wait_ld();
+                tmem_st_32x32b_x8(taddr + c0, zero);
                 if (j < p.n) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        if (c0 + c < rows)
-                            atomicAdd(out + static_cast<int64_t>(c0 + c) * p.n, __float2int_rn(__uint_as_float(v[c])));
+                    for (int cc = 0; cc < 8; ++cc)
+                        if (c0 + cc < rows)
+                            atomicAdd(out + static_cast<int64_t>(c0 + cc) * p.n, __float2int_rn(__uint_as_float(v[cc])));
                 }
             }
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8u * buf);
-            ++chunk_iter;
+            ++ch;
         }
     }
 
