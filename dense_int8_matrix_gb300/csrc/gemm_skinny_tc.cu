@@ -12,20 +12,22 @@
 // short row fragments cannot match (measured on GB300: 64-byte rows stream
 // at ~4.3 TB/s, 128-byte rows at ~6.5 TB/s, 256-byte rows at ~6.9 TB/s).
 //
-// Roles, per CTA (20 warps; warp 1 only owns the TMEM allocation):
+// Roles, per CTA (20 warps):
 //   warp 0      TMA: the int8 Bt boxes (128 rows x 256 B, 128-byte swizzle)
-//               into a 3-5-deep ring;
+//               into a 5-6-deep ring (it must cover the loaded HBM latency,
+//               ~2 us on GB300);
 //   warp 2      TMA: the f16 activation boxes (NP rows x 256 K) into a
-//               3-6-deep ring (they are re-read by every CTA and stay in L2);
+//               2-4-deep ring (they are re-read by every CTA and stay in L2);
 //   warps 4-11  two groups of four warps that take the stages in turn (one
 //               warp of a group per TMEM lane quarter): each lane reads its
-//               Bt row (256 int8) from shared memory, widens it to f16 in
-//               registers (exact) and writes it with tcgen05.st into one of
-//               three 128-column TMEM operand buffers; then one thread of the
-//               group issues the stage's tcgen05.mma (A from TMEM, B =
-//               activations from shared memory).  Two issuers keep the tensor
-//               pipe fed while each waits for its next stage.  Shared memory
-//               carries only the int8 bytes, read once;
+//               Bt row (256 int8) from shared memory, releases the stage,
+//               widens the row to f16 in registers (exact) and writes it with
+//               tcgen05.st into one of three 128-column TMEM operand buffers.
+//               Shared memory carries only the int8 bytes, read once;
+//   warps 1, 3  one thread each issues the tcgen05.mma of alternate stages
+//               (A from TMEM, B = activations from shared memory): a small-N
+//               MMA costs ~45 cycles of issue whatever N, so two issuers keep
+//               the tensor pipe fed while each waits for its next stage;
 //   warps 12-19 drain each accumulator chunk (two warps per lane quarter,
 //               half of the NP columns each), convert it to int32 (exact),
 //               add it into C (pre-zeroed) with coalesced integer atomics
@@ -63,8 +65,8 @@ struct SkCfg {
     // The activation ring must cover the MMA-to-refill latency (an L2 round
     // trip after the MMA two or more stages back completes); the Bt ring the
     // HBM latency.
-    static constexpr int BT_STAGES = NP >= 64 ? 3 : (NP >= 32 ? 4 : 5);
-    static constexpr int ACT_STAGES = NP >= 64 ? 3 : (NP >= 32 ? 4 : 6);
+    static constexpr int BT_STAGES = NP >= 32 ? 5 : 6;
+    static constexpr int ACT_STAGES = NP >= 64 ? 2 : 4;
     static constexpr int TMEM_COLS = 512;                      // 3 x 128 operand + 2 x NP accumulator
     static constexpr int EPI_COLS = NP / 2;                    // columns per epilogue warp
     static constexpr size_t SMEM =
@@ -214,10 +216,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             mbar_init(afree0 + 8u * b, 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf0 + 8u * b, kSkGroups);   // one arrival per widening group
+            mbar_init(accf0 + 8u * b, 2);   // one arrival per MMA issuer
             mbar_init(acce0 + 8u * b, kSkEpiWarps);
         }
-        mbar_init(done_bar, kSkGroups);
+        mbar_init(done_bar, 2);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -278,109 +280,104 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 wait_bounded(fullA0 + 8u * s, (last / Cfg::ACT_STAGES) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
             }
         }
-    } else if (warp >= kSkWidenWarp0 && warp < kSkEpiWarp0) {
-        // ------------------------------------------------- widen + MMA --
-        // Group g takes stages n = g, g + 2, ...  For each: widen the Bt rows
-        // into a TMEM operand buffer, sync the group, and one thread issues
-        // the stage's 16 MMAs into the chunk's accumulator (both groups add
-        // into the same, pre-zeroed accumulator: integer sums are order-free).
-        // At every chunk end each group arrives once on accf: by commit if it
-        // issued MMAs in the chunk, by a plain arrival otherwise.
-        const int q = warp & 3;
-        const int g = (warp - kSkWidenWarp0) >> 2;
-        const bool issuer = (q == 0) && (lane == 0);
-        const int row = q * 32 + lane;                // row of the 128-row Bt box
-        const uint32_t swz = row & 7;                 // 128-byte swizzle of this row
-        constexpr uint32_t idesc = idesc_f16(0u, 128, NP);
-        bool ok = true;
-        uint32_t ch = 0;            // chunk index of the current stage
-        bool issued_in_chunk = false;
-        bool acc_ready = false;     // this group has waited for the chunk's accumulator
-        Cursor c = cursor_at(p, lo);
-        uint32_t n = 0;
-        for (int64_t i = lo; i < hi; ++i, ++n, c.advance(p.num_sb)) {
-            const bool mine = (n & 1u) == static_cast<uint32_t>(g);
-            const uint32_t buf = ch & 1u;
-            if (mine && ok) {
-                const uint32_t s = n % Cfg::BT_STAGES, ph = (n / Cfg::BT_STAGES) & 1u;
-                const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
-                int got = 1;
-                if (lane == 0) {
-                    got = wait_bounded(fullB0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutEpilogue) &&
-                          wait_bounded(afree0 + 8u * b, bph ^ 1u, abort_flag, p.err, kDevErrTimeoutEpilogue);
-                }
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
-                    ok = false;
-                } else {
-                    tc_fence_after();
-                    // the row's 256 bytes: box 0 holds K 0..127, box 1 K 128..255
-                    uint4 v[16];
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------ MMA --
+        // Two issuers take the stages in turn (warp 1: even, warp 3: odd) and
+        // add into the chunk's pre-zeroed accumulator (integer sums are
+        // order-free), so one issues while the other waits.  At every chunk
+        // end each issuer arrives once on accf: by commit if it issued MMAs in
+        // the chunk, by a plain arrival otherwise.
+        if (lane == 0) {
+            const uint32_t g = warp == 1 ? 0u : 1u;
+            constexpr uint32_t idesc = idesc_f16(0u, 128, NP);
+            bool ok = true;
+            uint32_t ch = 0;
+            bool issued_in_chunk = false, acc_ready = false;
+            Cursor c = cursor_at(p, lo);
+            uint32_t n = 0;
+            for (int64_t i = lo; i < hi; ++i, ++n, c.advance(p.num_sb)) {
+                const uint32_t buf = ch & 1u;
+                if (ok && (n & 1u) == g) {
+                    const uint32_t sa = n % Cfg::ACT_STAGES, pha = (n / Cfg::ACT_STAGES) & 1u;
+                    const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
+                    ok = (acc_ready || wait_bounded(acce0 + 8u * buf, (ch >> 1) & 1u, abort_flag, p.err,
+                                                    kDevErrTimeoutMma)) &&
+                         wait_bounded(fullA0 + 8u * sa, pha, abort_flag, p.err, kDevErrTimeoutMma) &&
+                         wait_bounded(aready0 + 8u * b, bph, abort_flag, p.err, kDevErrTimeoutMma);
+                    if (ok) {
+                        acc_ready = true;
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem_acc + buf * NP;
+                        const uint32_t a_tmem = tmem_base + b * 128;
+                        const uint32_t act = sAct + sa * Cfg::ACT_STAGE;
 #pragma unroll
-                    for (int cc = 0; cc < 16; ++cc) {
-                        const uint32_t src = sBt + s * kSkBtStage + (cc >> 3) * kSkBtBox + row * 128;
-                        v[cc] = ld_shared_v4(src + (((cc & 7) ^ swz) << 4));
-                    }
-                    // the bytes are in registers: the stage can be refilled
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(emptyB0 + 8u * s);
-                    const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 128;
+                        for (int j = 0; j < kSkKbPerStage; ++j) {
+                            const uint64_t bdesc = smem_desc_sw128_kmajor(act + j * Cfg::ACT_BOX);
 #pragma unroll
-                    for (int hf = 0; hf < 8; ++hf) {
-                        uint32_t w[16];
-                        widen16(v[2 * hf], w);
-                        widen16(v[2 * hf + 1], w + 8);
-                        tmem_st_32x32b_x16(dst + hf * 16, w);
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    // the four warps of the group have written the buffer
-                    asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
-                    if (issuer) {
-                        const uint32_t sa = n % Cfg::ACT_STAGES, pha = (n / Cfg::ACT_STAGES) & 1u;
-                        bool ready = wait_bounded(fullA0 + 8u * sa, pha, abort_flag, p.err, kDevErrTimeoutMma);
-                        if (ready && !acc_ready)
-                            ready = wait_bounded(acce0 + 8u * buf, (ch >> 1) & 1u, abort_flag, p.err,
-                                                 kDevErrTimeoutMma);
-                        if (ready) {
-                            acc_ready = true;
-                            tc_fence_after();
-                            const uint32_t d_tmem = tmem_acc + buf * NP;
-                            const uint32_t a_tmem = tmem_base + b * 128;
-                            const uint32_t act = sAct + sa * Cfg::ACT_STAGE;
-#pragma unroll
-                            for (int j = 0; j < kSkKbPerStage; ++j) {
-                                const uint64_t bdesc = smem_desc_sw128_kmajor(act + j * Cfg::ACT_BOX);
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + 2u * kk, idesc, 1u);
-                            }
-                            mma_commit(afree0 + 8u * b);
-                            mma_commit(emptyA0 + 8u * sa);
-                            issued_in_chunk = true;
-                        } else {
-                            ok = false;
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + 2u * kk, idesc, 1u);
                         }
+                        mma_commit(afree0 + 8u * b);
+                        mma_commit(emptyA0 + 8u * sa);
+                        issued_in_chunk = true;
                     }
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                }
+                if (chunk_ends(p, c, i + 1 == hi)) {
+                    if (ok) {
+                        if (issued_in_chunk)
+                            mma_commit(accf0 + 8u * buf);
+                        else
+                            mbar_arrive(accf0 + 8u * buf);
+                    }
+                    issued_in_chunk = false;
+                    acc_ready = false;
+                    ++ch;
                 }
             }
-            if (chunk_ends(p, c, i + 1 == hi)) {
-                if (issuer && ok) {
-                    if (issued_in_chunk)
-                        mma_commit(accf0 + 8u * buf);
-                    else
-                        mbar_arrive(accf0 + 8u * buf);
-                }
-                issued_in_chunk = false;
-                acc_ready = false;
-                ++ch;
-            }
-        }
-        // Teardown: every MMA this group issued must complete before TMEM is freed.
-        if (issuer) {
+            // Teardown: every MMA issued must complete before TMEM is freed.
             mma_commit(done_bar);
             wait_bounded(done_bar, 0u, nullptr, p.err, kDevErrTimeoutTeardown);
+        }
+    } else if (warp >= kSkWidenWarp0 && warp < kSkEpiWarp0) {
+        // ---------------------------------------------------------- widen --
+        const int q = warp & 3;
+        const int g = (warp - kSkWidenWarp0) >> 2;   // this warp's group: stages n = g mod kSkGroups
+        const int row = q * 32 + lane;                // row of the 128-row Bt box
+        const uint32_t swz = row & 7;                 // 128-byte swizzle of this row
+        uint32_t n = g;
+        for (int64_t i = lo + g; i < hi; i += kSkGroups, n += kSkGroups) {
+            const uint32_t s = n % Cfg::BT_STAGES, ph = (n / Cfg::BT_STAGES) & 1u;
+            const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
+            int got = 1;
+            if (lane == 0) {
+                got = wait_bounded(fullB0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutEpilogue) &&
+                      wait_bounded(afree0 + 8u * b, bph ^ 1u, abort_flag, p.err, kDevErrTimeoutEpilogue);
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) break;
+            tc_fence_after();
+            // the row's 256 bytes: box 0 holds K 0..127, box 1 K 128..255
+            uint4 v[16];
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) {
+                const uint32_t src = sBt + s * kSkBtStage + (cc >> 3) * kSkBtBox + row * 128;
+                v[cc] = ld_shared_v4(src + (((cc & 7) ^ swz) << 4));
+            }
+            // the bytes are in registers: the stage can be refilled
+            __syncwarp();
+            if (lane == 0) mbar_arrive(emptyB0 + 8u * s);
+            const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * 128;
+#pragma unroll
+            for (int hf = 0; hf < 8; ++hf) {
+                uint32_t w[16];
+                widen16(v[2 * hf], w);
+                widen16(v[2 * hf + 1], w + 8);
+                tmem_st_32x32b_x16(dst + hf * 16, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(aready0 + 8u * b);
         }
     } else if (warp >= kSkEpiWarp0) {
         // ------------------------------------------------------- epilogue --
