@@ -82,6 +82,7 @@ struct SkParams {
     int num_sb;       // stages of 256 K per tile
     int tiles;        // ceil(n / 128)
     int64_t iters;    // tiles * num_sb
+    int iters32;      // iters * grid fits 32 bits
 };
 
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -145,8 +146,14 @@ __device__ __forceinline__ void widen16(const uint4 v, uint32_t* w) {
 }
 
 __device__ __forceinline__ void cta_range(const SkParams& p, int64_t& lo, int64_t& hi) {
-    lo = p.iters * blockIdx.x / gridDim.x;
-    hi = p.iters * (blockIdx.x + 1) / gridDim.x;
+    if (p.iters32) {   // iters * grid < 2^32: 32-bit arithmetic (cheaper at start-up)
+        const uint32_t it = static_cast<uint32_t>(p.iters);
+        lo = it * blockIdx.x / gridDim.x;
+        hi = it * (blockIdx.x + 1) / gridDim.x;
+    } else {
+        lo = p.iters * blockIdx.x / gridDim.x;
+        hi = p.iters * (blockIdx.x + 1) / gridDim.x;
+    }
 }
 
 // Position of an iteration: its 128-row tile and its stage within the tile,
@@ -163,8 +170,14 @@ struct Cursor {
 
 __device__ __forceinline__ Cursor cursor_at(const SkParams& p, int64_t i) {
     Cursor c;
-    c.tile = static_cast<int>(i / p.num_sb);
-    c.sb = static_cast<int>(i - static_cast<int64_t>(c.tile) * p.num_sb);
+    if (p.iters32) {
+        const uint32_t u = static_cast<uint32_t>(i);
+        c.tile = static_cast<int>(u / static_cast<uint32_t>(p.num_sb));
+        c.sb = static_cast<int>(u - static_cast<uint32_t>(c.tile) * static_cast<uint32_t>(p.num_sb));
+    } else {
+        c.tile = static_cast<int>(i / p.num_sb);
+        c.sb = static_cast<int>(i - static_cast<int64_t>(c.tile) * p.num_sb);
+    }
     return c;
 }
 
@@ -239,7 +252,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------- TMA: Bt --
         if (lane == 0) {
-            tma_prefetch_desc(&tmB);
             const uint64_t pol = policy_evict_first();
             uint32_t n_iss = 0;
             Cursor c = cursor_at(p, lo);
@@ -261,7 +273,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     } else if (warp == 2) {
         // ---------------------------------------------- TMA: activations --
         if (lane == 0) {
-            tma_prefetch_desc(&tmA);
             const uint64_t pol = policy_evict_last();
             uint32_t n_iss = 0;
             Cursor c = cursor_at(p, lo);
@@ -490,6 +501,7 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     p.iters = static_cast<int64_t>(p.tiles) * p.num_sb;
     int64_t grid = num_sms;
     if (grid > p.iters) grid = p.iters;
+    p.iters32 = (p.iters * (grid + 1)) < (int64_t(1) << 32) ? 1 : 0;
     auto kern = skinny_tc_kernel<NP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
