@@ -25,6 +25,7 @@ struct DeviceState {
     bool supported = false;
     int num_sms = 0;
     int* err_word = nullptr;
+    int tc2_pairs = 0;                // co-resident CTA pairs of the two-SM kernel
     cudaMemPool_t pool = nullptr;
 };
 
@@ -58,6 +59,7 @@ gemm_status device_state(DeviceState** out) {
             uint64_t keep = UINT64_MAX;  // keep freed scratch for the next call
             if (cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
                 return GEMM_ERR_CUDA;
+            s.tc2_pairs = tc2_max_pairs();
         }
         s.ready = true;
     }
@@ -103,8 +105,12 @@ gemm_status check_plan(const gemm_plan* p, int32_t dtype) {
     }
     if (p->path != GEMM_PATH_TENSOR) return GEMM_ERR_INVALID_ARG;
     // a plan may be edited to force a tile, but only to one that is compiled
-    if (p->bm != 64 && p->bm != 128) return GEMM_ERR_INVALID_ARG;
-    if (p->bn != 32 && p->bn != 64 && p->bn != 128 && p->bn != 256) return GEMM_ERR_INVALID_ARG;
+    if (p->bm == 256) {
+        if (p->bn != 256 || (p->grid % 2) != 0) return GEMM_ERR_INVALID_ARG;
+    } else {
+        if (p->bm != 64 && p->bm != 128) return GEMM_ERR_INVALID_ARG;
+        if (p->bn != 32 && p->bn != 64 && p->bn != 128 && p->bn != 256) return GEMM_ERR_INVALID_ARG;
+    }
     if (p->grid < 1 || p->k_pitch < p->k || (p->k_pitch % 8) != 0 || p->chunk_k < kTcBK ||
         (p->chunk_k % kTcBK) != 0)
         return GEMM_ERR_INVALID_ARG;
@@ -163,7 +169,7 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
         const int64_t num_kb = (p->k + kTcBK - 1) / kTcBK;
         const int64_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
         const int64_t capacity = static_cast<int64_t>(ds->num_sms) * tc_blocks_per_sm(p->bm, p->bn);
-        if (p->grid <= capacity) split = tc_tail_split(tiles, p->grid, nchunks, is_i8, &split_from);
+        if (p->grid <= capacity && p->bm != 256) split = tc_tail_split(tiles, p->grid, nchunks, is_i8, &split_from);
         if (split > 1 && tiles - split_from > kTcSplitFlagTiles) split = 1;
         if (split == 1) split_from = tiles;
     }
@@ -223,7 +229,7 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     cudaError_t e;
     {
         TraceScope t(GEMM_KERNEL_TC, stream);
-        e = launch_tc(L, stream);
+        e = p->bm == 256 ? launch_tc2(L, ds->tc2_pairs, stream) : launch_tc(L, stream);
     }
     if (ws) cudaFreeAsync(ws, stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -379,8 +385,13 @@ gemm_status gemm_trace_collect(float* ms_per_kind, int32_t* launches_per_kind) {
 gemm_status gemm_tc_kernel_info(int32_t bm, int32_t bn, int32_t dtype, int32_t* regs, int32_t* ctas_per_sm) {
     if (!regs || !ctas_per_sm) return GEMM_ERR_INVALID_ARG;
     if (dtype != GEMM_DTYPE_I8 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
-    *regs = tc_num_regs(bm, bn, dtype == GEMM_DTYPE_I8);
-    *ctas_per_sm = tc_occupancy(bm, bn, dtype == GEMM_DTYPE_I8);
+    if (bm == 256 && bn == 256) {
+        *regs = tc2_num_regs(dtype == GEMM_DTYPE_I8);
+        *ctas_per_sm = *regs > 0 ? 1 : 0;
+    } else {
+        *regs = tc_num_regs(bm, bn, dtype == GEMM_DTYPE_I8);
+        *ctas_per_sm = tc_occupancy(bm, bn, dtype == GEMM_DTYPE_I8);
+    }
     return *regs < 0 ? GEMM_ERR_INVALID_ARG : GEMM_OK;
 }
 

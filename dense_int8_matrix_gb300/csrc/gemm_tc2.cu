@@ -1,0 +1,459 @@
+// Two-SM tensor-core GEMM (tcgen05 cta_group::2) for large problems.
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 tile of C.  Each
+// CTA loads its own halves with TMA: 128 rows of A and 128 rows of Bt per
+// 64-element K step (no multicast); one tcgen05.mma.cta_group::2 (M = 256,
+// N = 256, K = 16), issued by the even CTA, reads the A rows of both CTAs
+// and the B rows of both CTAs and leaves each CTA's 128 rows of the result
+// in its own TMEM.  Per SM and K step that is 32 KB of operands through L2
+// and shared memory instead of 48 KB for a one-SM 128 x 256 tile with the
+// same output per SM, so the tensor pipe is fed more easily.  The TPU's
+// 256 x 256 multiply-accumulate array ("文章导读: Motivation for and Evaluation
+// of the First Tensor Processing Unit", section TPU介绍) has the same output
+// block size.
+//
+// Roles (both CTAs, 12 warps each):
+//   warp 0      TMA producer for this CTA's halves; the stage's "full"
+//               barrier lives in the even CTA, whose producer also announces
+//               the bytes of both CTAs;
+//   warp 1      TMEM allocation (cta_group::2, both CTAs); in the even CTA
+//               one lane issues the MMAs and commits with a multicast to
+//               both CTAs' barriers (stage free, accumulator full);
+//   warps 4-11  epilogue on this CTA's 128 rows, exactly as in the one-SM
+//               kernel (int8: drain each 1024-element K chunk to exact int32;
+//               TMA-store or vector-store C); releases the accumulator on the
+//               even CTA's barrier.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gemm {
+
+namespace {
+
+constexpr int kT2Stages = kTc2Stages;
+constexpr int kT2Half = 128;                      // rows of A and of Bt per CTA and K step
+constexpr int kT2HalfBytes = kT2Half * kTcRowBytes;
+constexpr int kT2StageBytes = 2 * kT2HalfBytes;   // this CTA's A and B halves
+constexpr int kT2Cols = 256;                      // N of the pair tile = TMEM columns per accumulator
+constexpr int kT2Half2 = kT2Cols / 2;             // columns per epilogue warp
+constexpr int kT2EpiBytes = kTcEpilogueWarps * kTcEpiStageBytes;
+constexpr size_t kT2Smem = static_cast<size_t>(kT2Stages) * kT2StageBytes + kT2EpiBytes + 1024 + 1024;
+static_assert(kT2Smem == tc2_smem_bytes(), "shared-memory size known to the planner");
+
+struct T2Params {
+    void* C;
+    int* err;
+    int64_t m, n;
+    int num_kb;
+    int chunk_kb;
+    int tiles_m, tiles_n, tiles;   // 256 x 256 tiles
+};
+
+constexpr int kBandM = 8;
+
+__device__ __forceinline__ void tile_coords2(int t, const T2Params& p, int& tm, int& tn) {
+    const int per_band = kBandM * p.tiles_n;
+    const int band = t / per_band;
+    const int first_m = band * kBandM;
+    const int rows_in_band = min(kBandM, p.tiles_m - first_m);
+    const int local = t - band * per_band;
+    tm = first_m + local % rows_in_band;
+    tn = local / rows_in_band;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the same shared location in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA load into this CTA's shared memory, completing on an mbarrier that may
+// live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* desc, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` (same offset) in both CTAs of the pair when the MMAs
+// issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
+}
+
+// Arrive on a barrier given by its shared::cluster address (possibly remote).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+template <bool INT_OUT, bool C_TMA>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const T2Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t sA = base;
+    const uint32_t sB = base + kT2Stages * kT2HalfBytes;
+    const uint32_t sEpi = base + kT2Stages * kT2StageBytes;
+    uint8_t* ctrl = smem_raw + (base - raw) + kT2Stages * kT2StageBytes + kT2EpiBytes;
+    const uint32_t bar0 = smem_u32(ctrl);
+    const uint32_t full_bar0 = bar0;                        // used in the even CTA
+    const uint32_t empty_bar0 = bar0 + 8u * kT2Stages;
+    const uint32_t accf_bar0 = bar0 + 16u * kT2Stages;
+    const uint32_t acce_bar0 = accf_bar0 + 16u;             // used in the even CTA
+    const uint32_t done_bar = acce_bar0 + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kT2Stages + 5));
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kT2Stages; ++s) {
+            mbar_init(full_bar0 + 8u * s, 1);
+            mbar_init(empty_bar0 + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar0 + 8u * b, 1);
+            mbar_init(acce_bar0 + 8u * b, 2 * kTcEpilogueWarps);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), 2 * kT2Cols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers and TMEM of both CTAs are ready
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer --
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_normal();
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < p.tiles; t += npairs) {
+                int tm, tn;
+                tile_coords2(t, p, tm, tn);
+                const int ya = tm * 256 + static_cast<int>(rank) * kT2Half;
+                const int yb = tn * 256 + static_cast<int>(rank) * kT2Half;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    const uint32_t s = issued % kT2Stages;
+                    const uint32_t ph = (issued / kT2Stages) & 1u;
+                    if (!wait_bounded(empty_bar0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    // both CTAs' copies complete on the even CTA's barrier,
+                    // which expects the bytes of both
+                    if (leader) mbar_arrive_expect_tx(full_bar0 + 8u * s, 2 * kT2StageBytes);
+                    const uint32_t fb = map_to_rank(full_bar0 + 8u * s, 0);
+                    tma_load_2d_pair(sA + s * kT2HalfBytes, &tmA, kb * kTcBK, ya, fb, pol);
+                    tma_load_2d_pair(sB + s * kT2HalfBytes, &tmB, kb * kTcBK, yb, fb, pol);
+                    ++issued;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------- MMA issuer (even CTA) --
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_f16(INT_OUT ? 0u : 1u, 256, kT2Cols);
+            uint32_t consumed = 0, acc_iter = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < p.tiles; t += npairs) {
+                for (int c0 = 0; ok && c0 < p.num_kb; c0 += p.chunk_kb) {
+                    const uint32_t buf = acc_iter & 1u;
+                    const uint32_t aph = (acc_iter >> 1) & 1u;
+                    if (!wait_bounded(acce_bar0 + 8u * buf, aph ^ 1u, abort_flag, p.err, kDevErrTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * kT2Cols;
+                    const int c1 = min(p.num_kb, c0 + p.chunk_kb);
+                    for (int kb = c0; kb < c1; ++kb) {
+                        const uint32_t s = consumed % kT2Stages;
+                        const uint32_t ph = (consumed / kT2Stages) & 1u;
+                        if (!wait_bounded(full_bar0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t adesc = smem_desc_sw128_kmajor(sA + s * kT2HalfBytes);
+                        const uint64_t bdesc = smem_desc_sw128_kmajor(sB + s * kT2HalfBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kTcBK / 16; ++kk)
+                            mma_f16_ss_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                            (kb > c0 || kk > 0) ? 1u : 0u);
+                        mma_commit_pair(empty_bar0 + 8u * s);
+                        ++consumed;
+                    }
+                    if (!ok) break;
+                    mma_commit_pair(accf_bar0 + 8u * buf);
+                    ++acc_iter;
+                }
+            }
+            mma_commit_pair(done_bar);
+            wait_bounded(done_bar, 0u, nullptr, p.err, kDevErrTimeoutTeardown);
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------------------- epilogue --
+        const int e = warp - 4;
+        const int q = warp & 3;
+        const int h = e >> 2;
+        uint32_t acc_iter = 0;
+        bool ok = true;
+        const int row_in_tile = q * 32 + lane;
+        const bool c_vec = ((p.n & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+        const uint32_t acce_leader = map_to_rank(acce_bar0, 0);
+        for (int t = pair; ok && t < p.tiles; t += npairs) {
+            int tm, tn;
+            tile_coords2(t, p, tm, tn);
+            const int64_t row0 = static_cast<int64_t>(tm) * 256 + static_cast<int64_t>(rank) * kT2Half;
+            const int64_t row = row0 + row_in_tile;
+            const int64_t col0 = static_cast<int64_t>(tn) * 256 + h * kT2Half2;
+            int32_t acc[INT_OUT ? kT2Half2 : 1];
+#pragma unroll
+            for (int j = 0; j < (INT_OUT ? kT2Half2 : 1); ++j) acc[j] = 0;
+            for (int c0 = 0; c0 < p.num_kb; c0 += p.chunk_kb) {
+                const uint32_t buf = acc_iter & 1u;
+                const uint32_t aph = (acc_iter >> 1) & 1u;
+                const bool last = c0 + p.chunk_kb >= p.num_kb;
+                int got = 1;
+                if (lane == 0)
+                    got = wait_bounded(accf_bar0 + 8u * buf, aph, abort_flag, p.err, kDevErrTimeoutEpilogue) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kT2Cols + h * kT2Half2;
+#pragma unroll
+                for (int sl = 0; sl < kT2Half2 / 32; ++sl) {
+                    uint32_t r[INT_OUT ? 1 : 32];
+                    if constexpr (INT_OUT) {
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            uint32_t v[16];
+                            tmem_ld_32x32b_x16(tcol + sl * 32 + hf * 16, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                acc[sl * 32 + hf * 16 + j] += __float2int_rn(__uint_as_float(v[j]));   // exact
+                        }
+                    } else {
+                        tmem_ld_32x32b_x32(tcol + sl * 32, r);
+                        tmem_wait_ld();
+                    }
+                    if (!last) continue;
+#define GEMM_TC2_OUT(j) (INT_OUT ? static_cast<uint32_t>(acc[(INT_OUT ? sl * 32 : 0) + (j)]) : r[INT_OUT ? 0 : (j)])
+                    const int64_t cs = col0 + sl * 32;
+                    if constexpr (C_TMA) {
+                        const uint32_t stg = sEpi + e * kTcEpiStageBytes;
+                        const uint32_t row_base = stg + lane * 128;
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            st_shared_v4(row_base + ((c ^ (lane & 7)) << 4), GEMM_TC2_OUT(4 * c), GEMM_TC2_OUT(4 * c + 1),
+                                         GEMM_TC2_OUT(4 * c + 2), GEMM_TC2_OUT(4 * c + 3));
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, stg, static_cast<int32_t>(cs), static_cast<int32_t>(row0 + q * 32));
+                            bulk_commit();
+                        }
+                    } else if (row < p.m) {
+                        uint32_t* out = static_cast<uint32_t*>(p.C) + row * p.n + cs;
+                        if (c_vec && cs + 32 <= p.n) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<uint4*>(out + j) =
+                                    make_uint4(GEMM_TC2_OUT(j), GEMM_TC2_OUT(j + 1), GEMM_TC2_OUT(j + 2), GEMM_TC2_OUT(j + 3));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (cs + j < p.n) out[j] = GEMM_TC2_OUT(j);
+                        }
+                    }
+#undef GEMM_TC2_OUT
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acce_leader + 8u * buf);
+                ++acc_iter;
+            }
+        }
+    }
+
+    if constexpr (C_TMA) {
+        if (warp >= 4 && lane == 0) bulk_wait_all();
+    }
+    tc_fence_before();
+    cluster_sync();   // the peer may still read this CTA's shared memory or barriers until here
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, 2 * kT2Cols);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool encode(CUtensorMap* map, CUtensorMapDataType type, void* ptr, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+            uint32_t box_inner, uint32_t box_rows) {
+    auto enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, type, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool INT_OUT, bool C_TMA>
+const void* tc2_kernel_ptr() {
+    return reinterpret_cast<const void*>(gemm_tc2_kernel<INT_OUT, C_TMA>);
+}
+
+cudaError_t configure2(const void* kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kT2Smem));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
+}  // namespace
+
+int tc2_max_pairs() {
+    const void* k = tc2_kernel_ptr<true, true>();
+    if (configure2(k) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = kT2Smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess) return 0;
+    return clusters;
+}
+
+cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
+    CUtensorMap mA, mB, mC;
+    std::memset(&mC, 0, sizeof(mC));
+    if (!encode(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<void*>(a.A16), a.k, a.m, a.k_pitch * 2, kTcBK, kT2Half))
+        return cudaErrorInvalidValue;
+    if (!encode(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<void*>(a.B16), a.k, a.n, a.k_pitch * 2, kTcBK, kT2Half))
+        return cudaErrorInvalidValue;
+    const bool c_tma = (a.n % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0;
+    if (c_tma && !encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.C, a.n, a.m, a.n * 4, 32, 32))
+        return cudaErrorInvalidValue;
+    T2Params p;
+    p.C = a.C;
+    p.err = a.err;
+    p.m = a.m;
+    p.n = a.n;
+    p.num_kb = static_cast<int>((a.k + kTcBK - 1) / kTcBK);
+    p.chunk_kb = a.chunk_kb;
+    p.tiles_m = static_cast<int>((a.m + 255) / 256);
+    p.tiles_n = static_cast<int>((a.n + 255) / 256);
+    p.tiles = p.tiles_m * p.tiles_n;
+    int pairs = a.grid / 2;
+    if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
+    if (pairs > p.tiles) pairs = p.tiles;
+    if (pairs < 1) pairs = 1;
+    const void* kern = a.int_out ? (c_tma ? tc2_kernel_ptr<true, true>() : tc2_kernel_ptr<true, false>())
+                                 : (c_tma ? tc2_kernel_ptr<false, true>() : tc2_kernel_ptr<false, false>());
+    cudaError_t e = configure2(kern);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = kT2Smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&mA, &mB, &mC, &p};
+    e = cudaLaunchKernelExC(&cfg, kern, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+int tc2_num_regs(bool int_out) {
+    cudaFuncAttributes attr;
+    const void* k = int_out ? tc2_kernel_ptr<true, true>() : tc2_kernel_ptr<false, true>();
+    if (cudaFuncGetAttributes(&attr, k) != cudaSuccess) return -1;
+    return attr.numRegs;
+}
+
+}  // namespace gemm

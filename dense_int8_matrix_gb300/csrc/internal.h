@@ -44,6 +44,15 @@ constexpr size_t tc_smem_bytes(int bm, int bn) {
            (tc_tma_store_tile(bm, bn) ? static_cast<size_t>(kTcEpilogueWarps) * kTcEpiStageBytes : 0) + 1024 + 1024;
 }
 
+// The two-SM tile (gemm_tc2.cu): a cluster of two CTAs computes 256 x 256 of
+// C; per CTA a 6-stage ring of 128-row A and Bt halves (32 KiB per stage) and
+// the same TMA-store epilogue staging as the wide one-SM tiles.
+constexpr int kTc2Stages = 6;
+constexpr size_t tc2_smem_bytes() {
+    return static_cast<size_t>(kTc2Stages) * 2 * 128 * kTcRowBytes +
+           static_cast<size_t>(kTcEpilogueWarps) * kTcEpiStageBytes + 1024 + 1024;
+}
+
 // Registers per thread the kernel is compiled for (launch bounds): wide
 // tiles keep 64-128 running sums per epilogue thread and run one CTA per SM;
 // narrow tiles fit two CTAs per SM.
@@ -92,6 +101,10 @@ struct TcLaunch {
 };
 
 cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream);
+// Two-SM kernel (bm = bn = 256); max_pairs = co-resident clusters (0: unknown).
+cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream);
+int tc2_max_pairs();
+int tc2_num_regs(bool int_out);
 // block_per_cu of a tile as the planner counts it (registers, shared memory,
 // TMEM); the tail split is used only when the whole grid fits at once.
 int tc_blocks_per_sm(int bm, int bn);

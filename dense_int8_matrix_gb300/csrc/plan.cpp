@@ -4,7 +4,9 @@
 //   claim 1 step 1 / claim 2  enumerate tiles the matrix unit can run: BM in
 //                             {64, 128} (M of one cta_group::1 MMA), BN in
 //                             {32, 64, 128, 256} (multiples of the minimum
-//                             N); K depth 64 16-bit elements per stage
+//                             N), plus the two-SM tile 256 x 256 (M of one
+//                             cta_group::2 MMA, run by a pair of CTAs); K
+//                             depth 64 16-bit elements per stage
 //   claim 3                   drop tiles whose shared memory or TMEM (two
 //                             accumulators of BN columns) exceed one SM
 //   claim 4 S1-S3             Thread_Blocks = output tiles; keep tiles with at
@@ -37,17 +39,25 @@ constexpr int64_t kMaxDim = 2147483647;
 struct Tile {
     int bm, bn;
 };
-constexpr Tile kTiles[] = {{64, 32}, {64, 64}, {64, 128}, {64, 256}, {128, 32}, {128, 64}, {128, 128}, {128, 256}};
+constexpr Tile kTiles[] = {{64, 32},  {64, 64},   {64, 128},  {64, 256}, {128, 32},
+                           {128, 64}, {128, 128}, {128, 256}, {256, 256}};
+
+bool is_pair(const Tile& t) { return t.bm == 256; }
+int64_t tile_smem(const Tile& t) {
+    return is_pair(t) ? static_cast<int64_t>(tc2_smem_bytes()) : static_cast<int64_t>(tc_smem_bytes(t.bm, t.bn));
+}
+// TMEM columns one CTA allocates: two accumulators of BN columns (the pair
+// tile: 256 columns per accumulator in each CTA)
+int64_t tile_tmem(const Tile& t) { return is_pair(t) ? 512 : tc_tmem_cols(t.bn); }
 constexpr int kNumTiles = sizeof(kTiles) / sizeof(kTiles[0]);
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-bool tile_fits(const Tile& t) {
-    return static_cast<int64_t>(tc_smem_bytes(t.bm, t.bn)) <= kSmemPerCtaMax &&
-           static_cast<int64_t>(tc_tmem_cols(t.bn)) <= kTmemColsPerSm;
-}
+bool tile_fits(const Tile& t) { return tile_smem(t) <= kSmemPerCtaMax && tile_tmem(t) <= kTmemColsPerSm; }
 
 int64_t out_tiles(const Tile& t, int64_t m, int64_t n) { return ceil_div(m, t.bm) * ceil_div(n, t.bn); }
+// Thread blocks (CTAs) of claim 4: two per tile for the pair tile.
+int64_t out_ctas(const Tile& t, int64_t m, int64_t n) { return out_tiles(t, m, n) * (is_pair(t) ? 2 : 1); }
 
 double tile_ratio(const Tile& t) {
     // flops of one K step over the bytes it stages: 2*BM*BN*BK / ((BM+BN)*BK*2)
@@ -56,8 +66,8 @@ double tile_ratio(const Tile& t) {
 
 int tile_bpc(const Tile& t) {
     const int64_t by_regs = kRegsPerSm / (static_cast<int64_t>(kTcThreads) * tc_regs_per_thread(t.bn));
-    const int64_t by_smem = kSmemPerSm / static_cast<int64_t>(tc_smem_bytes(t.bm, t.bn));
-    const int64_t by_tmem = kTmemColsPerSm / tc_tmem_cols(t.bn);
+    const int64_t by_smem = kSmemPerSm / tile_smem(t);
+    const int64_t by_tmem = kTmemColsPerSm / tile_tmem(t);
     int64_t b = by_regs;
     if (by_smem < b) b = by_smem;
     if (by_tmem < b) b = by_tmem;
@@ -115,10 +125,10 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
     // Step 3: keep tiles that fill every SM with at least one output tile.
     bool any_full = false;
     for (int i = 0; i < kNumTiles; ++i)
-        if (alive[i] && out_tiles(kTiles[i], m, n) >= num_sms) any_full = true;
+        if (alive[i] && out_ctas(kTiles[i], m, n) >= num_sms) any_full = true;
     if (any_full) {
         for (int i = 0; i < kNumTiles; ++i)
-            if (alive[i] && out_tiles(kTiles[i], m, n) < num_sms) alive[i] = false;
+            if (alive[i] && out_ctas(kTiles[i], m, n) < num_sms) alive[i] = false;
     } else {
         // Too small to fill the chip: only the smallest tile stays.
         int smallest = -1;
@@ -150,7 +160,7 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
     for (int i = 0; i < kNumTiles; ++i) {
         if (!alive[i]) continue;
         const Tile& t = kTiles[i];
-        const int64_t w = ceil_div(out_tiles(t, m, n), static_cast<int64_t>(num_sms) * tile_bpc(t));
+        const int64_t w = ceil_div(out_ctas(t, m, n), static_cast<int64_t>(num_sms) * tile_bpc(t));
         bool take = false;
         if (best < 0 || w < best_waves) {
             take = true;
@@ -178,7 +188,13 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
     p.tiles = static_cast<int32_t>(tiles);
     p.bpc = bpc;
     const int64_t slots = static_cast<int64_t>(num_sms) * bpc;
-    p.grid = static_cast<int32_t>(tiles < slots ? tiles : slots);
+    if (is_pair(t)) {
+        // CTAs in pairs: one pair per tile, at most one CTA per SM
+        const int64_t pairs = slots / 2;
+        p.grid = static_cast<int32_t>(2 * (tiles < pairs ? tiles : (pairs > 0 ? pairs : 1)));
+    } else {
+        p.grid = static_cast<int32_t>(tiles < slots ? tiles : slots);
+    }
     p.waves = static_cast<int32_t>(best_waves);
     p.ratio = tile_ratio(t);
     // Staged 16-bit rows need a 16-byte pitch for TMA.
@@ -196,7 +212,7 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
     // Beyond the five steps: split the last, partial wave along K.
     const int64_t nchunks = ceil_div(num_kb, p.chunk_k / kTcBK);
     int64_t split_from = tiles;
-    p.split_k = tc_tail_split(tiles, p.grid, nchunks, dtype == GEMM_DTYPE_I8, &split_from);
+    p.split_k = is_pair(t) ? 1 : tc_tail_split(tiles, p.grid, nchunks, dtype == GEMM_DTYPE_I8, &split_from);
     p.split_from = static_cast<int32_t>(split_from);
     *out = p;
     return GEMM_OK;

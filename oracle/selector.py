@@ -12,13 +12,16 @@ reading taken here:
 Step 1 (claim 1 step 1, claim 2): enumerate the thread-block tiles that the
     matrix unit can execute.  Tile sides are multiples of the unit's minimum
     shape ("TCUmin shape size"): BM in {64, 128} (the M of one tensor-core MMA
-    issued by one CTA) and BN in {32, 64, 128, 256}.  The K depth of a stage
-    is BK = 64 elements of a 16-bit operand (128 bytes, one swizzle row).
+    issued by one CTA) and BN in {32, 64, 128, 256}; and the 256 x 256 tile of
+    the two-SM MMA (M = 256), which a pair of thread blocks runs, each with
+    the resources of a (128, 256)-sized CTA.  The K depth of a stage is BK =
+    64 elements of a 16-bit operand (128 bytes, one swizzle row).
 Step 2 (claim 3): drop tiles whose resources do not fit one SM: shared memory
     of the CTA above the per-CTA limit, or a TMEM accumulator (two buffers of
     BN columns) above the 512 columns of an SM.
 Step 3 (claim 4 S1-S3): Thread_Blocks = ceil(m/BM) * ceil(n/BN) (the output
-    tiles); min_theory_block_num = the SM count.  Keep tiles with
+    tiles), twice that for the two-SM tile (two thread blocks per tile);
+    min_theory_block_num = the SM count.  Keep tiles with
     Thread_Blocks >= min_theory_block_num.  If none qualifies the problem is
     too small to fill the chip; "set the reuse counts to 1" is read as: keep
     only the smallest tile, (64, 32).
@@ -59,15 +62,24 @@ def regs_per_thread(bn: int) -> int:
     return 168 if bn >= 128 else 80
 
 
+def is_pair(bm: int, bn: int) -> bool:
+    return bm == 256
+
+
 def smem_per_cta(bm: int, bn: int) -> int:
     # operand ring + 1 KiB for aligning the ring to the 1024-byte swizzle
     # atom + 1 KiB for barriers and bookkeeping; wide tiles (BM = 128,
     # BN >= 128) also stage C for TMA stores in 8 buffers of 4 KiB
+    if is_pair(bm, bn):
+        # each CTA of the pair: 6 stages of 128-row A and B halves
+        return 6 * (128 + 128) * BK_ELEMS * ESIZE + 8 * 4096 + 1024 + 1024
     epilogue = 8 * 4096 if (bm == 128 and bn >= 128) else 0
     return STAGES * (bm + bn) * BK_ELEMS * ESIZE + epilogue + 1024 + 1024
 
 
 def tmem_cols(bn: int) -> int:
+    # two accumulators of BN columns per CTA (each CTA of a 256 x 256 pair
+    # holds two of its 128 x 256 halves: 512 columns)
     need = max(32, 2 * bn)
     cols = 32
     while cols < need:
@@ -81,6 +93,7 @@ def candidates():
     for bm in (64, 128):
         for bn in (32, 64, 128, 256):
             out.append((bm, bn))
+    out.append((256, 256))
     return out
 
 
@@ -93,9 +106,14 @@ def fits(bm: int, bn: int) -> bool:
     return True
 
 
-def thread_blocks(m: int, n: int, bm: int, bn: int) -> int:
-    """Step 3's Thread_Blocks: output tiles of the (m, n) result."""
+def tiles(m: int, n: int, bm: int, bn: int) -> int:
+    """Output tiles of the (m, n) result."""
     return math.ceil(m / bm) * math.ceil(n / bn)
+
+
+def thread_blocks(m: int, n: int, bm: int, bn: int) -> int:
+    """Step 3's Thread_Blocks: CTAs over all output tiles."""
+    return tiles(m, n, bm, bn) * (2 if is_pair(bm, bn) else 1)
 
 
 def ratio(bm: int, bn: int) -> float:
@@ -146,7 +164,7 @@ def select(dtype: str, m: int, k: int, n: int, num_sms: int) -> dict:
         "path": "tensor",
         "bm": bm,
         "bn": bn,
-        "tiles": thread_blocks(m, n, bm, bn),
+        "tiles": tiles(m, n, bm, bn),
         "bpc": blocks_per_sm(bm, bn),
         "waves": best_w,
         "fallback": fallback,

@@ -91,7 +91,7 @@ def test_workload_bf16_8192_sampled():
 
 # -------------------------------------------------- every compiled tile ----
 
-TILES = [(bm, bn) for bm in (64, 128) for bn in (32, 64, 128, 256)]
+TILES = [(bm, bn) for bm in (64, 128) for bn in (32, 64, 128, 256)] + [(256, 256)]
 
 
 def forced_plan(dtype, m, k, n, bm, bn, grid):
@@ -101,7 +101,7 @@ def forced_plan(dtype, m, k, n, bm, bn, grid):
 
 
 @pytest.mark.parametrize("bm,bn", TILES)
-@pytest.mark.parametrize("grid", [3, 1000])
+@pytest.mark.parametrize("grid", [4, 1000])
 def test_i8_every_tile(bm, bn, grid):
     # several tiles in both directions plus ragged tails; k = 2100 runs two
     # full 1024-element accumulator chunks and a ragged third one
@@ -117,7 +117,7 @@ def test_bf16_every_tile(bm, bn):
     m, k, n = 300, 1000, 700
     A = workloads.random_bf16((m, k), 103)
     Bt = workloads.random_bf16((n, k), 104)
-    p = forced_plan(B.GEMM_DTYPE_BF16, m, k, n, bm, bn, 5)
+    p = forced_plan(B.GEMM_DTYPE_BF16, m, k, n, bm, bn, 6)
     G.assert_bf16_close(A, Bt, G.gpu_bf16(A, Bt, plan=p))
 
 
@@ -254,6 +254,11 @@ def test_kernel_resources_match_planner(bm, bn):
     # co-schedules two such CTAs of this size; the planner counts registers,
     # shared memory and TMEM itself.)
     assumed = 168 if bn >= 128 else 80
+    if bm == 256:
+        for dtype in (B.GEMM_DTYPE_I8, B.GEMM_DTYPE_BF16):
+            regs, occ = B.gemm_tc_kernel_info(bm, bn, dtype)
+            assert 0 < regs <= assumed and occ >= 1
+        return
     for dtype in (B.GEMM_DTYPE_I8, B.GEMM_DTYPE_BF16):
         regs, occ = B.gemm_tc_kernel_info(bm, bn, dtype)
         assert 0 < regs <= assumed
@@ -333,3 +338,22 @@ def test_i8_skinny_extremes():
     C = G.gpu_i8(A, Bt)
     assert torch.all(C[:, 0::2] == 16384 * k)
     assert torch.all(C[:, 1::2] == -128 * 127 * k)
+
+
+@pytest.mark.parametrize("m,k,n,grid", [
+    (4096, 4096, 4096, 152), (1000, 3000, 777, 20), (513, 2100, 1500, 6), (257, 64, 300, 2),
+])
+def test_i8_two_sm_tile_shapes(m, k, n, grid):
+    # the 256 x 256 two-SM tile on ragged shapes and persistent grids
+    A = workloads.random_i8((m, k), m + 17)
+    Bt = workloads.random_i8((n, k), n + 19)
+    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, 256, 256, grid)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt, plan=p))
+
+
+@pytest.mark.parametrize("m,k,n", [(1000, 3000, 777), (512, 1024, 516)])
+def test_bf16_two_sm_tile_shapes(m, k, n):
+    A = workloads.random_bf16((m, k), m + 23)
+    Bt = workloads.random_bf16((n, k), n + 29)
+    p = forced_plan(B.GEMM_DTYPE_BF16, m, k, n, 256, 256, 8)
+    G.assert_bf16_close(A, Bt, G.gpu_bf16(A, Bt, plan=p))

@@ -49,4 +49,4 @@ def test_selector_ratio_closed_form():
 
 def test_every_candidate_fits():
     assert all(selector.fits(*c) for c in selector.candidates())
-    assert len(selector.candidates()) == 8
+    assert len(selector.candidates()) == 9
