@@ -47,6 +47,7 @@ struct NoAllocDevice {
     bool ready = false;
     bool supported = false;
     int num_sms = 0;
+    int tc2_pairs = 0;                  // co-resident pairs of the two-SM kernel
     unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch
     int* err = nullptr;                 // device address of g_noalloc_err
 };
@@ -76,6 +77,7 @@ gemm_status noalloc_device(NoAllocDevice** out) {
             p = nullptr;
             if (cudaGetSymbolAddress(&p, g_noalloc_err) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
             d.err = static_cast<int*>(p);
+            d.tc2_pairs = tc2_max_pairs();
         }
         d.ready = true;
     }
@@ -102,7 +104,8 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     if (skinny) {
         if (p->m > 64) return GEMM_ERR_INVALID_ARG;
     } else {
-        if (p->path != GEMM_PATH_TENSOR || (p->bm != 64 && p->bm != 128) ||
+        const bool pair_tile = p->bm == 256 && p->bn == 256 && (p->grid % 2) == 0;
+        if (p->path != GEMM_PATH_TENSOR || (!pair_tile && p->bm != 64 && p->bm != 128) ||
             (p->bn != 32 && p->bn != 64 && p->bn != 128 && p->bn != 256) || p->grid < 1 || p->k_pitch < p->k ||
             (p->k_pitch % 8) != 0 || p->chunk_k < kTcBK || (p->chunk_k % kTcBK) != 0 || p->chunk_k > kI8ChunkK)
             return GEMM_ERR_INVALID_ARG;
@@ -144,5 +147,6 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     L.split_from = 0;
     L.split_flags = nullptr;
     L.epoch = 0;
-    return launch_tc(L, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    const cudaError_t e = p->bm == 256 ? launch_tc2(L, d->tc2_pairs, stream) : launch_tc(L, stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
