@@ -159,37 +159,49 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     const bool need_stage = is_i8 || (p->k_pitch != p->k);
     const int chunk_kb = p->chunk_k / kTcBK;
 
-    // Tail split, recomputed for the tile and grid actually launched; only
-    // when every CTA of the grid can be resident at once (slices wait for
-    // slice 0 of their tile, which must be running).
+    // Tail split, recomputed for the tile and grid actually launched.  One-SM
+    // tiles: only when every CTA of the grid can be resident at once (slices
+    // wait for slice 0 of their tile, which must be running).  Two-SM tile:
+    // over the pairs launch_tc2 runs; its slices never wait on one another.
+    const bool pair_tile = p->bm == 256;
     const int64_t tiles = ((p->m + p->bm - 1) / p->bm) * ((p->n + p->bn - 1) / p->bn);
     int64_t split_from = tiles;
     int split = 1;
     {
         const int64_t num_kb = (p->k + kTcBK - 1) / kTcBK;
         const int64_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
-        const int64_t capacity = static_cast<int64_t>(ds->num_sms) * tc_blocks_per_sm(p->bm, p->bn);
-        if (p->grid <= capacity && p->bm != 256) split = tc_tail_split(tiles, p->grid, nchunks, is_i8, &split_from);
+        if (pair_tile) {
+            split = tc_tail_split(tiles, tc2_pairs_for(p->grid, ds->tc2_pairs, tiles), nchunks, is_i8, &split_from);
+        } else {
+            const int64_t capacity = static_cast<int64_t>(ds->num_sms) * tc_blocks_per_sm(p->bm, p->bn);
+            if (p->grid <= capacity) split = tc_tail_split(tiles, p->grid, nchunks, is_i8, &split_from);
+        }
         if (split > 1 && tiles - split_from > kTcSplitFlagTiles) split = 1;
         if (split == 1) split_from = tiles;
     }
-    // one flag per (split tile, epilogue warp), zeroed by the staging kernel
-    const int64_t flag_count = (tiles - split_from) * kTcEpilogueWarps;
+    // one-SM tiles: one flag per (split tile, epilogue warp); two-SM tile: one
+    // arrival counter per (split tile, CTA, epilogue warp) and the partial
+    // sums; flags and counters are zeroed by the staging kernel
+    const int64_t flag_count =
+        (tiles - split_from) * (pair_tile ? tc2_split_counters_per_tile() : kTcEpilogueWarps);
+    const int64_t partial_bytes = pair_tile ? (tiles - split_from) * tc2_split_ws_bytes_per_tile(split) : 0;
 
     void* ws = nullptr;
     const void* A16 = A;
     const void* B16 = Bt;
     int* flags = nullptr;
+    void* partials = nullptr;
     if (need_stage) {
         const int64_t a_bytes = ((p->m * p->k_pitch * 2 + 255) / 256) * 256;
         const int64_t b_bytes = ((p->n * p->k_pitch * 2 + 255) / 256) * 256;
         const int64_t f_bytes = ((flag_count * 4 + 255) / 256) * 256;
-        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes + f_bytes), ds->pool, stream) !=
-            cudaSuccess)
+        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes + f_bytes + partial_bytes), ds->pool,
+                                    stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
         uint16_t* Ah = static_cast<uint16_t*>(ws);
         uint16_t* Bh = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + a_bytes);
         if (flag_count > 0) flags = reinterpret_cast<int*>(static_cast<char*>(ws) + a_bytes + b_bytes);
+        if (partial_bytes > 0) partials = static_cast<char*>(ws) + a_bytes + b_bytes + f_bytes;
         cudaError_t e;
         {
             TraceScope t(GEMM_KERNEL_STAGE, stream);
@@ -226,6 +238,7 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     L.split_from = flags ? split_from : tiles;
     L.split_flags = flags;
     L.epoch = 1;
+    L.split_ws = partials;
     cudaError_t e;
     {
         TraceScope t(GEMM_KERNEL_TC, stream);

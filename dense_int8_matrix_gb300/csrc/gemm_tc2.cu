@@ -23,6 +23,14 @@
 //               kernel (int8: drain each 1024-element K chunk to exact int32;
 //               TMA-store or vector-store C); releases the accumulator on the
 //               even CTA's barrier.
+//
+// Tail split (int8 problems): when the last round of pairs is only partly
+// filled, the tiles of that round run as split_k K slices on otherwise idle
+// pairs.  Slices meet without waiting on one another: each epilogue warp
+// writes its exact int32 partial sums to a workspace slot and counts itself
+// on an atomic counter; the warp that arrives last adds the other slices'
+// partials and stores the tile.  No CTA ever waits on another, so the split
+// is correct whatever order or residency the pairs get.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,7 +61,16 @@ struct T2Params {
     int num_kb;
     int chunk_kb;
     int tiles_m, tiles_n, tiles;   // 256 x 256 tiles
+    int units;                     // split_from + (tiles - split_from) * split_k
+    int split_from;                // tiles [split_from, tiles) run as split_k K slices
+    int split_k;
+    uint32_t* split_cnt;           // per (split tile, CTA of the pair, epilogue warp): arrivals, zeroed
+    int4* split_ws;                // per counter: split_k slots of 32 x 128 int32 partial sums
 };
+
+// Partial sums of one epilogue warp: 32 rows x 128 columns, stored as int4
+// with lane-fastest order so that every warp access is one coalesced 512 B.
+constexpr int kT2SlotInt4 = 32 * kT2Half2 / 4;
 
 constexpr int kBandM = 8;
 
@@ -65,6 +82,37 @@ __device__ __forceinline__ void tile_coords2(int t, const T2Params& p, int& tm, 
     const int local = t - band * per_band;
     tm = first_m + local % rows_in_band;
     tn = local / rows_in_band;
+}
+
+// A unit of work: one tile over the K steps [kb_lo, kb_hi).  Units below
+// split_from are whole tiles; above it, the slices of a split tile are
+// consecutive units, each a run of whole accumulator chunks.
+struct Unit2 {
+    int tm, tn, kb_lo, kb_hi;
+    int split_tile;   // index among the split tiles, -1 if the tile is whole
+    int slice;
+};
+
+__device__ __forceinline__ Unit2 unit_at2(int u, const T2Params& p) {
+    Unit2 x;
+    int t;
+    if (u < p.split_from) {
+        t = u;
+        x.kb_lo = 0;
+        x.kb_hi = p.num_kb;
+        x.split_tile = -1;
+        x.slice = 0;
+    } else {
+        const int v = u - p.split_from;
+        x.split_tile = v / p.split_k;
+        x.slice = v - x.split_tile * p.split_k;
+        t = p.split_from + x.split_tile;
+        const int nch = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
+        x.kb_lo = (x.slice * nch / p.split_k) * p.chunk_kb;
+        x.kb_hi = min(p.num_kb, ((x.slice + 1) * nch / p.split_k) * p.chunk_kb);
+    }
+    tile_coords2(t, p, x.tm, x.tn);
+    return x;
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -133,6 +181,56 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
+// L2 load (bypassing L1) kept in program order, so that the fix-up reads one
+// 16-byte piece per lane at a time beside the 128 running sums
+__device__ __forceinline__ int4 ld_cg_v4(const int4* ptr) {
+    int4 v;
+    asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr)
+                 : "memory");
+    return v;
+}
+
+// Write one 32-column slice of this warp's 32 rows of C: each lane holds the
+// 32 values of its row.  With C_TMA, the lanes fill the warp's 128B-swizzled
+// 4 KiB staging buffer and one TMA store moves the 32 x 32 box (clipped at
+// the edges of C); otherwise each lane stores its row directly.
+template <bool C_TMA>
+__device__ __forceinline__ void store_slice32(const CUtensorMap* tmC, const T2Params& p, const uint32_t (&r)[32],
+                                              uint32_t stg, int lane, int row, int ytop, int cs, bool c_vec) {
+    if constexpr (C_TMA) {
+        const uint32_t row_base = stg + lane * 128;
+        if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            st_shared_v4(row_base + ((c ^ (lane & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, stg, cs, ytop);
+            bulk_commit();
+        }
+    } else if (row < p.m) {
+        uint32_t* out = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row) * p.n + cs;
+        if (c_vec && cs + 32 <= p.n) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) *reinterpret_cast<uint4*>(out + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (cs + j < p.n) out[j] = r[j];
+        }
+    }
+}
+
 template <bool INT_OUT, bool C_TMA>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -188,12 +286,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t pol = policy_evict_normal();
             uint32_t issued = 0;
             bool ok = true;
-            for (int t = pair; ok && t < p.tiles; t += npairs) {
-                int tm, tn;
-                tile_coords2(t, p, tm, tn);
-                const int ya = tm * 256 + static_cast<int>(rank) * kT2Half;
-                const int yb = tn * 256 + static_cast<int>(rank) * kT2Half;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+            for (int u = pair; ok && u < p.units; u += npairs) {
+                const Unit2 w = unit_at2(u, p);
+                const int ya = w.tm * 256 + static_cast<int>(rank) * kT2Half;
+                const int yb = w.tn * 256 + static_cast<int>(rank) * kT2Half;
+                for (int kb = w.kb_lo; kb < w.kb_hi; ++kb) {
                     const uint32_t s = issued % kT2Stages;
                     const uint32_t ph = (issued / kT2Stages) & 1u;
                     if (!wait_bounded(empty_bar0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) {
@@ -216,8 +313,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             constexpr uint32_t idesc = idesc_f16(INT_OUT ? 0u : 1u, 256, kT2Cols);
             uint32_t consumed = 0, acc_iter = 0;
             bool ok = true;
-            for (int t = pair; ok && t < p.tiles; t += npairs) {
-                for (int c0 = 0; ok && c0 < p.num_kb; c0 += p.chunk_kb) {
+            for (int u = pair; ok && u < p.units; u += npairs) {
+                const Unit2 w = unit_at2(u, p);
+                for (int c0 = w.kb_lo; ok && c0 < w.kb_hi; c0 += p.chunk_kb) {
                     const uint32_t buf = acc_iter & 1u;
                     const uint32_t aph = (acc_iter >> 1) & 1u;
                     if (!wait_bounded(acce_bar0 + 8u * buf, aph ^ 1u, abort_flag, p.err, kDevErrTimeoutMma)) {
@@ -226,7 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kT2Cols;
-                    const int c1 = min(p.num_kb, c0 + p.chunk_kb);
+                    const int c1 = min(w.kb_hi, c0 + p.chunk_kb);
                     for (int kb = c0; kb < c1; ++kb) {
                         const uint32_t s = consumed % kT2Stages;
                         const uint32_t ph = (consumed / kT2Stages) & 1u;
@@ -262,19 +360,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row_in_tile = q * 32 + lane;
         const bool c_vec = ((p.n & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         const uint32_t acce_leader = map_to_rank(acce_bar0, 0);
-        for (int t = pair; ok && t < p.tiles; t += npairs) {
-            int tm, tn;
-            tile_coords2(t, p, tm, tn);
-            const int64_t row0 = static_cast<int64_t>(tm) * 256 + static_cast<int64_t>(rank) * kT2Half;
-            const int64_t row = row0 + row_in_tile;
-            const int64_t col0 = static_cast<int64_t>(tn) * 256 + h * kT2Half2;
+        const uint32_t stg = sEpi + e * kTcEpiStageBytes;
+        for (int u = pair; ok && u < p.units; u += npairs) {
+            const Unit2 w = unit_at2(u, p);
+            // 32-bit coordinates, as in the TMA boxes (m, n < 2^31 - 256)
+            const int row0 = w.tm * 256 + static_cast<int>(rank) * kT2Half;
+            const int row = row0 + row_in_tile;
+            const int col0 = w.tn * 256 + h * kT2Half2;
+            const int ytop = row0 + q * 32;
+            // int8 problems: exact int32 running sums over the K chunks
             int32_t acc[INT_OUT ? kT2Half2 : 1];
 #pragma unroll
             for (int j = 0; j < (INT_OUT ? kT2Half2 : 1); ++j) acc[j] = 0;
-            for (int c0 = 0; c0 < p.num_kb; c0 += p.chunk_kb) {
+            for (int c0 = w.kb_lo; c0 < w.kb_hi; c0 += p.chunk_kb) {
                 const uint32_t buf = acc_iter & 1u;
                 const uint32_t aph = (acc_iter >> 1) & 1u;
-                const bool last = c0 + p.chunk_kb >= p.num_kb;
+                const bool last = c0 + p.chunk_kb >= w.kb_hi;
                 int got = 1;
                 if (lane == 0)
                     got = wait_bounded(accf_bar0 + 8u * buf, aph, abort_flag, p.err, kDevErrTimeoutEpilogue) ? 1 : 0;
@@ -285,60 +386,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kT2Cols + h * kT2Half2;
+                if constexpr (INT_OUT) {
+                    // drain the chunk into the running sums, then free the
+                    // accumulator before any output work
 #pragma unroll
-                for (int sl = 0; sl < kT2Half2 / 32; ++sl) {
-                    uint32_t r[INT_OUT ? 1 : 32];
-                    if constexpr (INT_OUT) {
+                    for (int sl = 0; sl < kT2Half2 / 16; ++sl) {
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(tcol + sl * 16, v);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            uint32_t v[16];
-                            tmem_ld_32x32b_x16(tcol + sl * 32 + hf * 16, v);
-                            tmem_wait_ld();
+                        for (int j = 0; j < 16; ++j)
+                            acc[sl * 16 + j] += __float2int_rn(__uint_as_float(v[j]));   // exact
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(acce_leader + 8u * buf);
+                    ++acc_iter;
+                    if (!last) continue;
+                    if (w.split_tile >= 0) {
+                        // this warp's 32 x 128 region of a split tile
+                        const int64_t region =
+                            (static_cast<int64_t>(w.split_tile) * 2 + rank) * kTcEpilogueWarps + e;
+                        int4* slots = p.split_ws + region * p.split_k * kT2SlotInt4;
+                        int4* mine = slots + w.slice * kT2SlotInt4;
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                acc[sl * 32 + hf * 16 + j] += __float2int_rn(__uint_as_float(v[j]));   // exact
+                        for (int j = 0; j < kT2Half2 / 4; ++j)
+                            __stcg(mine + j * 32 + lane, make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+                        __threadfence();
+                        __syncwarp();
+                        uint32_t before = 0;
+                        if (lane == 0) before = atomic_add_acq_rel_gpu(p.split_cnt + region, 1u);
+                        before = __shfl_sync(0xffffffffu, before, 0);
+                        if (before + 1u != static_cast<uint32_t>(p.split_k)) continue;   // another slice finishes the tile
+                        __threadfence();
+#pragma unroll
+                        for (int s = 0; s < kTcMaxSplit; ++s) {
+                            if (s >= p.split_k) break;
+                            if (s == w.slice) continue;
+                            const int4* other = slots + s * kT2SlotInt4;
+#pragma unroll
+                            for (int j = 0; j < kT2Half2 / 4; ++j) {
+                                const int4 x = ld_cg_v4(other + j * 32 + lane);
+                                acc[4 * j] += x.x;
+                                acc[4 * j + 1] += x.y;
+                                acc[4 * j + 2] += x.z;
+                                acc[4 * j + 3] += x.w;
+                            }
                         }
-                    } else {
+                    }
+#pragma unroll
+                    for (int sl = 0; sl < kT2Half2 / 32; ++sl) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = static_cast<uint32_t>(acc[sl * 32 + j]);
+                        store_slice32<C_TMA>(&tmC, p, r, stg, lane, row, ytop, col0 + sl * 32, c_vec);
+                    }
+                } else {
+                    // fp32 results (one chunk): load and store 32 columns at a time
+#pragma unroll
+                    for (int sl = 0; sl < kT2Half2 / 32; ++sl) {
+                        uint32_t r[32];
                         tmem_ld_32x32b_x32(tcol + sl * 32, r);
                         tmem_wait_ld();
+                        if (last) store_slice32<C_TMA>(&tmC, p, r, stg, lane, row, ytop, col0 + sl * 32, c_vec);
                     }
-                    if (!last) continue;
-#define GEMM_TC2_OUT(j) (INT_OUT ? static_cast<uint32_t>(acc[(INT_OUT ? sl * 32 : 0) + (j)]) : r[INT_OUT ? 0 : (j)])
-                    const int64_t cs = col0 + sl * 32;
-                    if constexpr (C_TMA) {
-                        const uint32_t stg = sEpi + e * kTcEpiStageBytes;
-                        const uint32_t row_base = stg + lane * 128;
-                        if (lane == 0) bulk_wait_read_all();
-                        __syncwarp();
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            st_shared_v4(row_base + ((c ^ (lane & 7)) << 4), GEMM_TC2_OUT(4 * c), GEMM_TC2_OUT(4 * c + 1),
-                                         GEMM_TC2_OUT(4 * c + 2), GEMM_TC2_OUT(4 * c + 3));
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmC, stg, static_cast<int32_t>(cs), static_cast<int32_t>(row0 + q * 32));
-                            bulk_commit();
-                        }
-                    } else if (row < p.m) {
-                        uint32_t* out = static_cast<uint32_t*>(p.C) + row * p.n + cs;
-                        if (c_vec && cs + 32 <= p.n) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                *reinterpret_cast<uint4*>(out + j) =
-                                    make_uint4(GEMM_TC2_OUT(j), GEMM_TC2_OUT(j + 1), GEMM_TC2_OUT(j + 2), GEMM_TC2_OUT(j + 3));
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (cs + j < p.n) out[j] = GEMM_TC2_OUT(j);
-                        }
-                    }
-#undef GEMM_TC2_OUT
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(acce_leader + 8u * buf);
+                    ++acc_iter;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(acce_leader + 8u * buf);
-                ++acc_iter;
             }
         }
     }
@@ -382,6 +498,14 @@ cudaError_t configure2(const void* kern) {
 
 }  // namespace
 
+int tc2_pairs_for(int grid, int max_pairs, int64_t tiles) {
+    int64_t pairs = grid / 2;
+    if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
+    if (pairs > tiles) pairs = tiles;
+    if (pairs < 1) pairs = 1;
+    return static_cast<int>(pairs);
+}
+
 int tc2_max_pairs() {
     const void* k = tc2_kernel_ptr<true, true>();
     if (configure2(k) != cudaSuccess) return 0;
@@ -422,10 +546,15 @@ cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
     p.tiles_m = static_cast<int>((a.m + 255) / 256);
     p.tiles_n = static_cast<int>((a.n + 255) / 256);
     p.tiles = p.tiles_m * p.tiles_n;
-    int pairs = a.grid / 2;
-    if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
-    if (pairs > p.tiles) pairs = p.tiles;
-    if (pairs < 1) pairs = 1;
+    const int pairs = tc2_pairs_for(a.grid, max_pairs, p.tiles);
+    // the split was planned for this number of pairs; units only reorder the
+    // work, so any pair count stays correct
+    const bool split = a.int_out && a.split_k > 1 && a.split_flags && a.split_ws && a.split_from < p.tiles;
+    p.split_k = split ? a.split_k : 1;
+    p.split_from = split ? static_cast<int>(a.split_from) : p.tiles;
+    p.units = p.split_from + (p.tiles - p.split_from) * p.split_k;
+    p.split_cnt = split ? reinterpret_cast<uint32_t*>(a.split_flags) : nullptr;
+    p.split_ws = split ? static_cast<int4*>(a.split_ws) : nullptr;
     const void* kern = a.int_out ? (c_tma ? tc2_kernel_ptr<true, true>() : tc2_kernel_ptr<true, false>())
                                  : (c_tma ? tc2_kernel_ptr<false, true>() : tc2_kernel_ptr<false, false>());
     cudaError_t e = configure2(kern);

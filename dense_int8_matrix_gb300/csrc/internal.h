@@ -96,14 +96,24 @@ struct TcLaunch {
     bool int_out;         // true: int8 problem (f16 operands, int32 output)
     int split_k;          // K slices of the tail tiles (1 = none)
     int64_t split_from;   // first split tile
-    int* split_flags;     // (tiles - split_from) * kTcEpilogueWarps ints, zeroed (device)
-    uint32_t epoch;       // launch epoch written to / awaited in split_flags
+    int* split_flags;     // one-SM tiles: (tiles - split_from) * kTcEpilogueWarps flags; two-SM tile:
+                          // (tiles - split_from) * tc2_split_counters_per_tile() counters; zeroed (device)
+    uint32_t epoch;       // launch epoch written to / awaited in split_flags (one-SM tiles)
+    void* split_ws = nullptr;   // two-SM tile: tc2_split_ws_bytes_per_tile(split_k) bytes per split tile
 };
 
 cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream);
 // Two-SM kernel (bm = bn = 256); max_pairs = co-resident clusters (0: unknown).
 cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream);
 int tc2_max_pairs();
+// Pairs launch_tc2 runs for a planned grid of 2 * pairs CTAs.
+int tc2_pairs_for(int grid, int max_pairs, int64_t tiles);
+// Tail split of the two-SM kernel: arrival counters and partial-sum bytes per
+// split tile (two CTAs x eight epilogue warps, each 32 x 128 int32 per slice).
+constexpr int tc2_split_counters_per_tile() { return 2 * kTcEpilogueWarps; }
+constexpr int64_t tc2_split_ws_bytes_per_tile(int split_k) {
+    return static_cast<int64_t>(split_k) * 2 * kTcEpilogueWarps * 32 * 128 * 4;
+}
 int tc2_num_regs(bool int_out);
 // block_per_cu of a tile as the planner counts it (registers, shared memory,
 // TMEM); the tail split is used only when the whole grid fits at once.

@@ -165,28 +165,35 @@ def test_status_strings(lib):
     (2048, 2048, 1536, 148, 2, 148),     # 192 = 148 + 44; 148 // 44 = 3, but only 2 K chunks
     (1024, 4096, 4096, 148, 1, 256),     # 256 = 148 + 108; 148 // 108 = 1: no split
     (1000, 777, 3000, 148, 1, 192),      # one K chunk: nothing to split
-    (4096, 4096, 4096, 152, 1, 256),     # the two-SM tile: no tail split
+    (4096, 4096, 4096, 152, 2, 228),     # two-SM tile: 256 tiles = 3 * 76 pairs + 28; 76 // 28 = 2
+    (8192, 8192, 8192, 152, 2, 988),     # two-SM tile: 1024 = 13 * 76 + 36; 76 // 36 = 2
+    (2048, 1024, 2560, 148, 1, 80),      # two-SM tile: 80 tiles on 74 pairs, 74 // 6 = 12 but 1 K chunk
 ])
 def test_tail_split_fields(lib, m, k, n, sms, split, split_from):
     p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, m, k, n, sms)
-    if p.bm == 256:   # the two-SM tile runs without a tail split
-        assert p.split_k == 1 and p.split_from == p.tiles
-        return
     tiles = p.tiles
-    full = (tiles // p.grid) * p.grid
+    workers = p.grid // 2 if p.bm == 256 else p.grid   # CTA pairs for the two-SM tile
+    full = (tiles // workers) * workers
     tail = tiles - full
     want = 1
-    if tiles > p.grid and tail:
+    if tiles > workers and tail:
         nch = -(-(-(-k // 64)) // 16)
-        want = min(p.grid // tail, nch, 8)
+        want = min(workers // tail, nch, 8)
         if want < 2:
             want = 1
     assert p.split_k == want
+    operands = (m * p.k_pitch * 2 + 255) // 256 * 256 + (n * p.k_pitch * 2 + 255) // 256 * 256
     if want > 1:
         assert (p.split_k, p.split_from) == (split, split_from)
-        assert p.split_from + (tiles - p.split_from) * p.split_k <= full + p.grid
+        assert p.split_from + (tiles - p.split_from) * p.split_k <= full + workers
+        words = (tiles - p.split_from) * (16 if p.bm == 256 else 8)
+        extra = (words * 4 + 255) // 256 * 256
+        if p.bm == 256:   # partial sums: split_k slots of 256 x 256 int32 per split tile
+            extra += (tiles - p.split_from) * p.split_k * 256 * 256 * 4
+        assert p.workspace_bytes == operands + extra
     else:
         assert p.split_from == tiles
+        assert p.workspace_bytes == operands
     pb = B.gemm_plan_for_sms(B.GEMM_DTYPE_BF16, m, k, n, sms)
     assert pb.split_k == 1 and pb.split_from == pb.tiles
 

@@ -351,6 +351,31 @@ def test_i8_two_sm_tile_shapes(m, k, n, grid):
     G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt, plan=p))
 
 
+@pytest.mark.parametrize("k,n,grid,split", [
+    (4100, 1500, 14, 2),    # 24 tiles = 3 x 7 pairs + 3 -> 3 tiles in 2 K slices
+    (4100, 1500, 22, 5),    # 2 x 11 + 2 -> 2 tiles in 5 slices (the last one a single K step)
+    (4100, 1500, 46, 5),    # 23 + 1, capped by the 5 K chunks
+    (8200, 1500, 46, 8),    # 9 K chunks: capped at 8 slices
+    (4100, 1498, 14, 2),    # n % 4 != 0: direct stores of C
+])
+def test_i8_two_sm_tail_split_exact(k, n, grid, split):
+    # two-SM tiles of the last, partial round split along K over idle pairs:
+    # every slice writes its partial sums, the last to arrive adds and stores
+    m = 1000
+    A = workloads.random_i8((m, k), 51)
+    Bt = workloads.random_i8((n, k), 52)
+    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, 256, 256, grid)
+    tiles = -(-m // 256) * -(-n // 256)
+    pairs = grid // 2
+    nch = -(-(-(-k // 64)) // 16)
+    assert min(pairs // (tiles - tiles // pairs * pairs), nch, 8) == split
+    C1 = G.gpu_i8(A, Bt, plan=p)
+    G.assert_i8_exact(A, Bt, C1)
+    C2 = G.gpu_i8(A, Bt, plan=p)    # again: the counters start from zero every launch
+    assert torch.equal(C1, C2)
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
 @pytest.mark.parametrize("m,k,n", [(1000, 3000, 777), (512, 1024, 516)])
 def test_bf16_two_sm_tile_shapes(m, k, n):
     A = workloads.random_bf16((m, k), m + 23)
