@@ -103,8 +103,8 @@ def load():
         "gemm_i8_run_host": [P, vp, vp, vp, vp],
         "gemm_bf16_run_host": [P, vp, vp, vp, vp],
         "gemm_device_error": [vp, ctypes.POINTER(i32)],
-        "gemm_trace_begin": [i32],
-        "gemm_trace_collect": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)],
+        "gemm_trace_begin": [i32, i32],
+        "gemm_trace_collect": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "gemm_tc_kernel_info": [i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "gemm_selftest_wait_timeout": [i32, vp],
         "gemm_i8_run_noalloc": [P, vp, vp, vp, vp],
@@ -233,16 +233,17 @@ def gemm_device_error(stream=None):
     return st, code.value
 
 
-def gemm_trace_begin(capacity: int) -> None:
-    _check(load().gemm_trace_begin(capacity), "gemm_trace_begin")
+def gemm_trace_begin(capacity: int, every: int = 1) -> None:
+    _check(load().gemm_trace_begin(capacity, every), "gemm_trace_begin")
 
 
 def gemm_trace_collect():
-    """([ms per kernel kind], [launches per kernel kind])."""
+    """Per kind: (summed ms of the timed units, timed units, launches counted)."""
     ms = (ctypes.c_float * GEMM_KERNEL_KINDS)()
+    timed = (ctypes.c_int32 * GEMM_KERNEL_KINDS)()
     cnt = (ctypes.c_int32 * GEMM_KERNEL_KINDS)()
-    _check(load().gemm_trace_collect(ms, cnt), "gemm_trace_collect")
-    return list(ms), list(cnt)
+    _check(load().gemm_trace_collect(ms, timed, cnt), "gemm_trace_collect")
+    return list(ms), list(timed), list(cnt)
 
 
 def gemm_tc_kernel_info(bm: int, bn: int, dtype: int):

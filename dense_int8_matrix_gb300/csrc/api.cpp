@@ -68,6 +68,8 @@ gemm_status device_state(DeviceState** out) {
 }
 
 // ---------------------------------------------------------------- tracing --
+// While tracing is on, every kernel launch is counted per kind, and every
+// `every`-th run call ("sampled") records CUDA events around its launches.
 struct TraceRec {
     int kind;
     cudaEvent_t start, stop;
@@ -75,13 +77,30 @@ struct TraceRec {
 
 std::mutex g_trace_mu;
 bool g_trace_on = false;
+int32_t g_trace_every = 1;
+int64_t g_trace_calls = 0;
+int32_t g_trace_launches[GEMM_KERNEL_KINDS] = {};
 std::vector<TraceRec> g_trace;
 size_t g_trace_used = 0;
 
+// Whether this run call is sampled (decided once per call).
+bool trace_sample_call() {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (!g_trace_on) return false;
+    return (g_trace_calls++ % g_trace_every) == 0;
+}
+
+void trace_count(int kind) {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (g_trace_on) ++g_trace_launches[kind];
+}
+
+// Events around the launches made in this scope, if the call is sampled.
 struct TraceScope {
     TraceRec* rec = nullptr;
     cudaStream_t stream;
-    TraceScope(int kind, cudaStream_t s) : stream(s) {
+    TraceScope(int kind, cudaStream_t s, bool sampled) : stream(s) {
+        if (!sampled) return;
         std::lock_guard<std::mutex> lock(g_trace_mu);
         if (g_trace_on && g_trace_used < g_trace.size()) {
             rec = &g_trace[g_trace_used++];
@@ -127,31 +146,37 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     if (!ds->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
     if (!tensor_map_encoder_available() && p->path == GEMM_PATH_TENSOR) return GEMM_ERR_CUDA;
 
+    const bool sampled = trace_sample_call();
     if (p->path == GEMM_PATH_SKINNY) {
         if (skinny_tc_supported(p->m, p->n, p->k, A, Bt) && tensor_map_encoder_available()) {
             // f16 copy of the small activation matrix; the same launch zeroes C,
-            // which the tensor-core kernel adds its partial sums into
+            // which the tensor-core kernel adds its partial sums into.  The
+            // skinny kernel starts while the staging kernel runs (programmatic
+            // dependent launch), so the two are timed as one unit.
             void* ws = nullptr;
             const size_t a_bytes = static_cast<size_t>(p->m * p->k * 2);
             if (cudaMallocFromPoolAsync(&ws, a_bytes, ds->pool, stream) != cudaSuccess) return GEMM_ERR_CUDA;
             cudaError_t e;
             {
-                TraceScope t(GEMM_KERNEL_STAGE, stream);
+                TraceScope t(GEMM_KERNEL_SKINNY, stream, sampled);
                 e = launch_stage_i8(static_cast<const int8_t*>(A), nullptr, static_cast<uint16_t*>(ws), nullptr, p->m, 0,
                                     p->k, p->k, static_cast<int*>(C), p->m * p->n, ds->num_sms, stream);
-            }
-            if (e == cudaSuccess) {
-                TraceScope t(GEMM_KERNEL_SKINNY, stream);
-                e = launch_skinny_tc(static_cast<const int8_t*>(Bt), static_cast<const uint16_t*>(ws),
-                                     static_cast<int32_t*>(C), ds->err_word, p->m, p->n, p->k, ds->num_sms, stream);
+                if (e == cudaSuccess) {
+                    trace_count(GEMM_KERNEL_STAGE);
+                    e = launch_skinny_tc(static_cast<const int8_t*>(Bt), static_cast<const uint16_t*>(ws),
+                                         static_cast<int32_t*>(C), ds->err_word, p->m, p->n, p->k, ds->num_sms,
+                                         stream);
+                    if (e == cudaSuccess) trace_count(GEMM_KERNEL_SKINNY);
+                }
             }
             cudaFreeAsync(ws, stream);
             return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
         }
-        TraceScope t(GEMM_KERNEL_SKINNY, stream);
+        TraceScope t(GEMM_KERNEL_SKINNY, stream, sampled);
         if (launch_skinny_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), static_cast<int32_t*>(C),
                              p->m, p->n, p->k, ds->num_sms, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
+        trace_count(GEMM_KERNEL_SKINNY);
         return GEMM_OK;
     }
 
@@ -204,7 +229,7 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
         if (partial_bytes > 0) partials = static_cast<char*>(ws) + a_bytes + b_bytes + f_bytes;
         cudaError_t e;
         {
-            TraceScope t(GEMM_KERNEL_STAGE, stream);
+            TraceScope t(GEMM_KERNEL_STAGE, stream, sampled);
             if (is_i8)
                 e = launch_stage_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), Ah, Bh, p->m, p->n,
                                     p->k, p->k_pitch, flags, flag_count, ds->num_sms, stream);
@@ -216,6 +241,7 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
             cudaFreeAsync(ws, stream);
             return GEMM_ERR_CUDA;
         }
+        trace_count(GEMM_KERNEL_STAGE);
         A16 = Ah;
         B16 = Bh;
     }
@@ -241,9 +267,10 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     L.split_ws = partials;
     cudaError_t e;
     {
-        TraceScope t(GEMM_KERNEL_TC, stream);
+        TraceScope t(GEMM_KERNEL_TC, stream, sampled);
         e = p->bm == 256 ? launch_tc2(L, ds->tc2_pairs, stream) : launch_tc(L, stream);
     }
+    if (e == cudaSuccess) trace_count(GEMM_KERNEL_TC);
     if (ws) cudaFreeAsync(ws, stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -352,8 +379,8 @@ gemm_status gemm_device_error(void* stream, int32_t* code) {
     return GEMM_ERR_TIMEOUT;
 }
 
-gemm_status gemm_trace_begin(int32_t capacity) {
-    if (capacity < 0) return GEMM_ERR_INVALID_ARG;
+gemm_status gemm_trace_begin(int32_t capacity, int32_t every) {
+    if (capacity < 0 || every < 1) return GEMM_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_trace_mu);
     while (g_trace.size() < static_cast<size_t>(capacity)) {
         TraceRec r;
@@ -366,16 +393,20 @@ gemm_status gemm_trace_begin(int32_t capacity) {
         g_trace.push_back(r);
     }
     g_trace_used = 0;
+    g_trace_every = every;
+    g_trace_calls = 0;
+    for (int i = 0; i < GEMM_KERNEL_KINDS; ++i) g_trace_launches[i] = 0;
     g_trace_on = true;
     return GEMM_OK;
 }
 
-gemm_status gemm_trace_collect(float* ms_per_kind, int32_t* launches_per_kind) {
-    if (!ms_per_kind || !launches_per_kind) return GEMM_ERR_INVALID_ARG;
+gemm_status gemm_trace_collect(float* ms_per_kind, int32_t* timed_per_kind, int32_t* launches_per_kind) {
+    if (!ms_per_kind || !timed_per_kind || !launches_per_kind) return GEMM_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_trace_mu);
     for (int i = 0; i < GEMM_KERNEL_KINDS; ++i) {
         ms_per_kind[i] = 0.f;
-        launches_per_kind[i] = 0;
+        timed_per_kind[i] = 0;
+        launches_per_kind[i] = g_trace_launches[i];
     }
     gemm_status st = GEMM_OK;
     for (size_t i = 0; i < g_trace_used; ++i) {
@@ -387,7 +418,7 @@ gemm_status gemm_trace_collect(float* ms_per_kind, int32_t* launches_per_kind) {
         }
         if (r.kind >= 0 && r.kind < GEMM_KERNEL_KINDS) {
             ms_per_kind[r.kind] += ms;
-            launches_per_kind[r.kind] += 1;
+            timed_per_kind[r.kind] += 1;
         }
     }
     g_trace_on = false;

@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     } else if (warp == 2) {
         // ---------------------------------------------- TMA: activations --
         if (lane == 0) {
+            pdl_wait();   // the activations are written by the staging kernel just before
             const uint64_t pol = policy_evict_last();
             uint32_t n_iss = 0;
             Cursor c = cursor_at(p, lo);
@@ -417,6 +418,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             mbar_arrive(acce0);
             mbar_arrive(acce0 + 8u);
         }
+        pdl_wait();   // C is zeroed by the staging kernel just before
         uint32_t ch = 0;
         Cursor c = cursor_at(p, lo);
         for (int64_t i = lo; i < hi; ++i, c.advance(p.num_sb)) {
@@ -505,7 +507,23 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     auto kern = skinny_tc_kernel<NP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(grid), kSkThreads, Cfg::SMEM, stream>>>(mB, mA, p);
+    // Programmatic dependent launch: the kernel may start while the staging
+    // kernel before it runs.  Bt is not written by that kernel (which itself
+    // started after all earlier work in the stream), so its stream starts at
+    // once; the activation loads and the writes of C wait for it.
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kSkThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mB, mA, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

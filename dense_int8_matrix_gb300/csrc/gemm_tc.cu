@@ -192,6 +192,9 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the epilogue writes C and the split flags only after the kernel before
+    // this one in the stream (programmatic dependent launch)
+    if (warp >= 4) pdl_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer --
@@ -199,6 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
             if (C_TMA) tma_prefetch_desc(&tmC);
+            pdl_wait();   // the operands may come from the staging kernel just before
             const uint64_t pol = policy_evict_normal();
             uint32_t issued = 0;
             bool ok = true;
@@ -517,7 +521,21 @@ cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     auto kern = c_tma ? gemm_tc_kernel<BM, BN, INT_OUT, Cfg::TMA_STORE> : gemm_tc_kernel<BM, BN, INT_OUT, false>;
     cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<a.grid, kTcThreads, Cfg::SMEM, stream>>>(mA, mB, mC, p);
+    // programmatic dependent launch: set-up overlaps the kernel before; every
+    // global access waits for it (pdl_wait)
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(a.grid), 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer --
         if (lane == 0) {
+            pdl_wait();   // the operands may come from the staging kernel just before
             const uint64_t pol = policy_evict_normal();
             uint32_t issued = 0;
             bool ok = true;
@@ -352,6 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp >= 4) {
         // -------------------------------------------------------- epilogue --
+        pdl_wait();   // C and the split counters are written only after the kernel before
         const int e = warp - 4;
         const int q = warp & 3;
         const int h = e >> 2;
@@ -561,17 +563,21 @@ cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: set-up overlaps the kernel before; every
+    // global access waits for it (pdl_wait)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = kT2Smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     void* args[] = {&mA, &mB, &mC, &p};
     e = cudaLaunchKernelExC(&cfg, kern, args);
     if (e != cudaSuccess) return e;

@@ -29,6 +29,15 @@ enum DeviceErrorCode : int {
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s
 constexpr uint32_t kWaitIterCap = 1u << 28;
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running: it may set up (barriers, TMEM, descriptors) and read memory that
+// kernel does not write, but must call pdl_wait() before anything else; the
+// wait returns once the earlier kernel has completed and its writes are
+// visible.  pdl_launch_dependents() lets such a dependent start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -16,6 +16,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace gemm {
 
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restr
                                                             uint4* __restrict__ dstB, int64_t itemsA,
                                                             int64_t itemsB, int* __restrict__ zero,
                                                             int64_t zero_count) {
+    pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
     const int64_t total = itemsA + itemsB;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_count; i += stride)
@@ -89,6 +91,7 @@ __global__ void __launch_bounds__(256) stage_i8_rows_kernel(const int8_t* __rest
                                                             __half* __restrict__ Bh, int64_t m, int64_t n, int64_t k,
                                                             int64_t k_pitch, int* __restrict__ zero,
                                                             int64_t zero_count) {
+    pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
     const int64_t totalA = m * k;
     const int64_t total = totalA + n * k;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -108,6 +111,7 @@ __global__ void __launch_bounds__(256) stage_b16_rows_kernel(const uint16_t* __r
                                                              const uint16_t* __restrict__ Bt,
                                                              uint16_t* __restrict__ Ah, uint16_t* __restrict__ Bh,
                                                              int64_t m, int64_t n, int64_t k, int64_t k_pitch) {
+    pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
     const int64_t totalA = m * k;
     const int64_t total = totalA + n * k;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;

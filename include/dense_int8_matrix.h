@@ -201,14 +201,22 @@ gemm_status gemm_bf16_run_host(const gemm_plan *plan, const uint16_t *A, const u
 gemm_status gemm_device_error(void *stream, int32_t *code);
 
 /*
- * Tracing: while enabled, every kernel launch made by gemm_*_run records a
- * pair of CUDA events around itself on the launch stream (at most
- * `capacity` launches are recorded).  gemm_trace_collect waits for them and
- * writes, per GEMM_KERNEL_* kind, the summed device time in ms and the
- * launch count (arrays of GEMM_KERNEL_KINDS entries), then disables tracing.
+ * Tracing.  While enabled, every kernel launch made by gemm_*_run is counted
+ * per GEMM_KERNEL_* kind, and every `every`-th gemm_*_run call (the first,
+ * the (every+1)-th, ...) records a pair of CUDA events on its stream around
+ * each timed unit (at most `capacity` units are recorded): the staging
+ * launch and the GEMM launch of the tensor path separately (kinds STAGE and
+ * TC); on the skinny tensor-core path the staging launch and the skinny
+ * launch together, as kind SKINNY, because the skinny kernel starts while
+ * the staging kernel runs (programmatic dependent launch).  Calls that are
+ * not sampled record no events, so sampling keeps the timing from slowing
+ * the work it measures.  gemm_trace_collect waits for the events and writes,
+ * per kind (arrays of GEMM_KERNEL_KINDS entries): the summed device time in
+ * ms of the timed units, the number of timed units, and the number of
+ * launches counted; it then disables tracing.  every >= 1.
  */
-gemm_status gemm_trace_begin(int32_t capacity);
-gemm_status gemm_trace_collect(float *ms_per_kind, int32_t *launches_per_kind);
+gemm_status gemm_trace_begin(int32_t capacity, int32_t every);
+gemm_status gemm_trace_collect(float *ms_per_kind, int32_t *timed_per_kind, int32_t *launches_per_kind);
 
 /* Registers per thread and CTAs per SM of the compiled tensor-core kernel for
  * a tile (-1 / 0 if no such kernel); needs a device. */

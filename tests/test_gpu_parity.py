@@ -236,14 +236,23 @@ def test_trace_counts_launches():
     B.gemm_trace_begin(16)
     for _ in range(3):
         B.gemm_i8_run(p, dA, dB, C)
-    ms, cnt = B.gemm_trace_collect()
+    ms, timed, cnt = B.gemm_trace_collect()
     assert cnt[B.GEMM_KERNEL_STAGE] == 3 and cnt[B.GEMM_KERNEL_TC] == 3
-    assert ms[B.GEMM_KERNEL_TC] > 0
+    assert timed == [3, 3, 0] and ms[B.GEMM_KERNEL_TC] > 0
+    # sampled: calls 0, 4 and 8 of 10 are timed, all launches counted
+    B.gemm_trace_begin(16, 4)
+    for _ in range(10):
+        B.gemm_i8_run(p, dA, dB, C)
+    ms, timed, cnt = B.gemm_trace_collect()
+    assert cnt == [10, 10, 0] and timed == [3, 3, 0]
+    G.assert_i8_exact(dA.cpu(), dB.cpu(), C.cpu())
+    # skinny tensor-core path: staging and skinny launches timed as one unit
     ps = B.gemm_i8_plan(16, k, n)
     B.gemm_trace_begin(4)
-    B.gemm_i8_run(ps, dA[:16].contiguous(), dB, C[:16].contiguous())
-    ms, cnt = B.gemm_trace_collect()
-    assert cnt == [1, 0, 1]     # f16 copy of A (and zeroing of C), then the skinny kernel
+    Cs = torch.empty((16, n), dtype=torch.int32, device="cuda")
+    B.gemm_i8_run(ps, dA[:16].contiguous(), dB, Cs)
+    ms, timed, cnt = B.gemm_trace_collect()
+    assert cnt == [1, 0, 1] and timed == [0, 0, 1] and ms[B.GEMM_KERNEL_SKINNY] > 0
 
 
 @pytest.mark.parametrize("bm,bn", TILES)
