@@ -52,6 +52,12 @@ constexpr int kSkBtBox = 128 * 128;                  // one 128 B x 128-row box
 constexpr int kSkBtStage = 2 * kSkBtBox;             // 256 B x 128 rows
 constexpr int kSkGroups = 2;                         // widening groups (4 warps each)
 constexpr int kSkAbufs = 3;                          // TMEM operand buffers, 128 columns each
+// Barriers that two alternating warps (issuers or widening groups) would wait
+// on at alternate phases are kept apart instead: a parity wait can only tell
+// two neighbouring phases apart, so every barrier must have one waiter
+// sequence.  Operand-buffer barriers are indexed by stage mod 6 (buffer x
+// issuer), the Bt ring's "full" barriers by stage mod 2 x ring depth.
+constexpr int kSkAbufBars = 2 * kSkAbufs;
 constexpr int kSkEpiWarps = 8;
 constexpr int kSkWidenWarp0 = 4;
 constexpr int kSkEpiWarp0 = kSkWidenWarp0 + 4 * kSkGroups;
@@ -199,32 +205,31 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const uint32_t sAct = base + Cfg::BT_STAGES * kSkBtStage;
     uint8_t* ctrl = smem_raw + (base - raw) + Cfg::BT_STAGES * kSkBtStage + Cfg::ACT_STAGES * Cfg::ACT_STAGE;
     const uint32_t bar0 = smem_u32(ctrl);
-    const uint32_t fullB0 = bar0;                              // [BT_STAGES]
-    const uint32_t emptyB0 = fullB0 + 8u * Cfg::BT_STAGES;     // [BT_STAGES]
+    constexpr uint32_t kFullB = 2 * Cfg::BT_STAGES;           // "full" barriers of the Bt ring
+    const uint32_t fullB0 = bar0;                              // [2 * BT_STAGES], stage n: n % (2 * BT_STAGES)
+    const uint32_t emptyB0 = fullB0 + 8u * kFullB;             // [BT_STAGES], stage n: n % BT_STAGES
     const uint32_t fullA0 = emptyB0 + 8u * Cfg::BT_STAGES;     // [ACT_STAGES]
     const uint32_t emptyA0 = fullA0 + 8u * Cfg::ACT_STAGES;    // [ACT_STAGES]
-    const uint32_t aready0 = emptyA0 + 8u * Cfg::ACT_STAGES;   // [kSkAbufs]
-    const uint32_t afree0 = aready0 + 8u * kSkAbufs;           // [kSkAbufs]
-    const uint32_t accf0 = afree0 + 8u * kSkAbufs;             // [2]
+    const uint32_t aready0 = emptyA0 + 8u * Cfg::ACT_STAGES;   // [kSkAbufBars], stage n: n % 6
+    const uint32_t afree0 = aready0 + 8u * kSkAbufBars;        // [kSkAbufBars], stage n: n % 6
+    const uint32_t accf0 = afree0 + 8u * kSkAbufBars;          // [2]
     const uint32_t acce0 = accf0 + 16u;                        // [2]
     const uint32_t done_bar = acce0 + 16u;
-    uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * Cfg::BT_STAGES + 2 * Cfg::ACT_STAGES + 2 * kSkAbufs + 5));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(
+        ctrl + 8 * (kFullB + Cfg::BT_STAGES + 2 * Cfg::ACT_STAGES + 2 * kSkAbufBars + 5));
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < Cfg::BT_STAGES; ++s) {
-            mbar_init(fullB0 + 8u * s, 1);
-            mbar_init(emptyB0 + 8u * s, 4);   // the four warps of the widening group
-        }
+        for (uint32_t s = 0; s < kFullB; ++s) mbar_init(fullB0 + 8u * s, 1);
+        for (int s = 0; s < Cfg::BT_STAGES; ++s) mbar_init(emptyB0 + 8u * s, 4);   // the widening group's warps
         for (int s = 0; s < Cfg::ACT_STAGES; ++s) {
             mbar_init(fullA0 + 8u * s, 1);
             mbar_init(emptyA0 + 8u * s, 1);   // the MMA's commit
         }
-        for (int b = 0; b < kSkAbufs; ++b) {
+        for (int b = 0; b < kSkAbufBars; ++b) {
             mbar_init(aready0 + 8u * b, 4);
             mbar_init(afree0 + 8u * b, 1);
         }
@@ -261,14 +266,15 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 const int tile = c.tile;
                 const int x = c.sb * 256;
                 const uint32_t dst = sBt + s * kSkBtStage;
-                mbar_arrive_expect_tx(fullB0 + 8u * s, kSkBtStage);
-                tma_load_2d(dst, &tmB, x, tile * 128, fullB0 + 8u * s, pol);
-                tma_load_2d(dst + kSkBtBox, &tmB, x + 128, tile * 128, fullB0 + 8u * s, pol);
+                const uint32_t fb = fullB0 + 8u * (n_iss % kFullB);
+                mbar_arrive_expect_tx(fb, kSkBtStage);
+                tma_load_2d(dst, &tmB, x, tile * 128, fb, pol);
+                tma_load_2d(dst + kSkBtBox, &tmB, x + 128, tile * 128, fb, pol);
             }
-            for (uint32_t s = 0; s < static_cast<uint32_t>(Cfg::BT_STAGES) && s < n_iss; ++s) {
-                const uint32_t last = s + ((n_iss - 1u - s) / Cfg::BT_STAGES) * Cfg::BT_STAGES;
-                wait_bounded(fullB0 + 8u * s, (last / Cfg::BT_STAGES) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
-            }
+            // the last BT_STAGES copies may still be in flight (earlier ones
+            // landed before their slot was reused)
+            for (uint32_t j = n_iss > static_cast<uint32_t>(Cfg::BT_STAGES) ? n_iss - Cfg::BT_STAGES : 0u; j < n_iss; ++j)
+                wait_bounded(fullB0 + 8u * (j % kFullB), (j / kFullB) & 1u, nullptr, p.err, kDevErrTimeoutTeardown);
         }
     } else if (warp == 2) {
         // ---------------------------------------------- TMA: activations --
@@ -311,11 +317,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 const uint32_t buf = ch & 1u;
                 if (ok && (n & 1u) == g) {
                     const uint32_t sa = n % Cfg::ACT_STAGES, pha = (n / Cfg::ACT_STAGES) & 1u;
-                    const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
+                    const uint32_t b = n % kSkAbufs;
+                    const uint32_t rb = n % kSkAbufBars, rph = (n / kSkAbufBars) & 1u;
                     ok = (acc_ready || wait_bounded(acce0 + 8u * buf, (ch >> 1) & 1u, abort_flag, p.err,
                                                     kDevErrTimeoutMma)) &&
                          wait_bounded(fullA0 + 8u * sa, pha, abort_flag, p.err, kDevErrTimeoutMma) &&
-                         wait_bounded(aready0 + 8u * b, bph, abort_flag, p.err, kDevErrTimeoutMma);
+                         wait_bounded(aready0 + 8u * rb, rph, abort_flag, p.err, kDevErrTimeoutMma);
                     if (ok) {
                         acc_ready = true;
                         tc_fence_after();
@@ -329,12 +336,19 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                             for (int kk = 0; kk < 4; ++kk)
                                 mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + 2u * kk, idesc, 1u);
                         }
-                        mma_commit(afree0 + 8u * b);
+                        mma_commit(afree0 + 8u * rb);
                         mma_commit(emptyA0 + 8u * sa);
                         issued_in_chunk = true;
                     }
                 }
                 if (chunk_ends(p, c, i + 1 == hi)) {
+                    // An issuer with no stage in this chunk still arrives, but
+                    // only once the epilogue has drained this accumulator's
+                    // previous chunk: otherwise its (immediate) arrival could
+                    // complete that earlier phase before the other issuer's
+                    // MMAs into it have finished.
+                    if (ok && !acc_ready)
+                        ok = wait_bounded(acce0 + 8u * buf, (ch >> 1) & 1u, abort_flag, p.err, kDevErrTimeoutMma);
                     if (ok) {
                         if (issued_in_chunk)
                             mma_commit(accf0 + 8u * buf);
@@ -358,12 +372,18 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const uint32_t swz = row & 7;                 // 128-byte swizzle of this row
         uint32_t n = g;
         for (int64_t i = lo + g; i < hi; i += kSkGroups, n += kSkGroups) {
-            const uint32_t s = n % Cfg::BT_STAGES, ph = (n / Cfg::BT_STAGES) & 1u;
-            const uint32_t b = n % kSkAbufs, bph = (n / kSkAbufs) & 1u;
+            const uint32_t s = n % Cfg::BT_STAGES;
+            const uint32_t b = n % kSkAbufs;
             int got = 1;
             if (lane == 0) {
-                got = wait_bounded(fullB0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutEpilogue) &&
-                      wait_bounded(afree0 + 8u * b, bph ^ 1u, abort_flag, p.err, kDevErrTimeoutEpilogue);
+                got = wait_bounded(fullB0 + 8u * (n % kFullB), (n / kFullB) & 1u, abort_flag, p.err,
+                                   kDevErrTimeoutEpilogue);
+                // buffer b last held stage n - 3: its MMAs must be complete
+                if (got && n >= static_cast<uint32_t>(kSkAbufs)) {
+                    const uint32_t pn = n - kSkAbufs;
+                    got = wait_bounded(afree0 + 8u * (pn % kSkAbufBars), (pn / kSkAbufBars) & 1u, abort_flag, p.err,
+                                       kDevErrTimeoutEpilogue);
+                }
             }
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) break;
@@ -389,7 +409,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(aready0 + 8u * b);
+            if (lane == 0) mbar_arrive(aready0 + 8u * (n % kSkAbufBars));
         }
     } else if (warp >= kSkEpiWarp0) {
         // ------------------------------------------------------- epilogue --

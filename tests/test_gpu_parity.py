@@ -339,6 +339,27 @@ def test_i8_skinny_tensor_core_shapes(m, k, n):
     G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
 
 
+@pytest.mark.parametrize("m,k,n", [(1, 8192, 8192), (16, 8192, 8192), (64, 8192, 8192), (5, 3328, 2000)])
+def test_i8_skinny_repeat_stress(m, k, n):
+    # many back-to-back launches: the kernel's barrier protocol (two MMA
+    # issuers and two widening groups sharing TMEM buffers and accumulators)
+    # must neither time out nor mix phases under any timing
+    A = workloads.random_i8((m, k), 61 + m)
+    Bt = workloads.random_i8((n, k), 62 + m)
+    C0 = G.gpu_i8(A, Bt)
+    G.assert_i8_exact(A, Bt, C0)
+    dA, dB = A.cuda(), Bt.cuda()
+    p = B.gemm_i8_plan(m, k, n)
+    outs = [torch.empty((m, n), dtype=torch.int32, device="cuda") for _ in range(8)]
+    ref = C0.cuda()
+    for it in range(400):
+        B.gemm_i8_run(p, dA, dB, outs[it % 8])
+        if it % 8 == 7:
+            for o in outs:
+                assert torch.equal(o, ref)
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
 def test_i8_skinny_extremes():
     m, k, n = 64, 16384, 1000
     A = torch.full((m, k), -128, dtype=torch.int8)
