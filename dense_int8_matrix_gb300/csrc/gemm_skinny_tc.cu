@@ -223,6 +223,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int lane = threadIdx.x & 31;
 
     if (warp == 0 && lane == 0) {
+        // the descriptors are fetched while the CTA sets up
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmA);
         for (uint32_t s = 0; s < kFullB; ++s) mbar_init(fullB0 + 8u * s, 1);
         for (int s = 0; s < Cfg::BT_STAGES; ++s) mbar_init(emptyB0 + 8u * s, 4);   // the widening group's warps
         for (int s = 0; s < Cfg::ACT_STAGES; ++s) {

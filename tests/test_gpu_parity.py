@@ -360,6 +360,29 @@ def test_i8_skinny_repeat_stress(m, k, n):
     assert B.gemm_device_error() == (B.GEMM_OK, 0)
 
 
+def test_i8_skinny_two_streams():
+    # skinny GEMMs running at the same time on two streams (each call takes
+    # its own scratch from the stream-ordered pool) must not disturb each other
+    shapes = [(16, 8192, 4096), (40, 4096, 8192)]
+    data = []
+    for i, (m, k, n) in enumerate(shapes):
+        A = workloads.random_i8((m, k), 91 + i)
+        Bt = workloads.random_i8((n, k), 93 + i)
+        want = torch.from_numpy(oracle.gemm_i8(A.numpy(), Bt.numpy()))
+        data.append((B.gemm_i8_plan(m, k, n), A.cuda(), Bt.cuda(), want,
+                     [torch.empty((m, n), dtype=torch.int32, device="cuda") for _ in range(4)]))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for it in range(40):
+        for (p, dA, dB, _, outs), s in zip(data, streams):
+            B.gemm_i8_run(p, dA, dB, outs[it % 4], s)
+    torch.cuda.synchronize()
+    for (_, _, _, want, outs) in data:
+        for o in outs:
+            assert torch.equal(o.cpu(), want)
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
 def test_i8_skinny_extremes():
     m, k, n = 64, 16384, 1000
     A = torch.full((m, k), -128, dtype=torch.int8)
