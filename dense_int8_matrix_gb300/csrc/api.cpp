@@ -119,7 +119,7 @@ gemm_status check_plan(const gemm_plan* p, int32_t dtype) {
     if (!p || p->version != GEMM_PLAN_VERSION || p->dtype != dtype) return GEMM_ERR_INVALID_ARG;
     if (p->m < 1 || p->k < 1 || p->n < 1) return GEMM_ERR_INVALID_ARG;
     if (p->path == GEMM_PATH_SKINNY) {
-        if (dtype != GEMM_DTYPE_I8 || p->m > 64 || p->grid < 1) return GEMM_ERR_INVALID_ARG;
+        if (dtype != GEMM_DTYPE_I8 || p->m > 128 || p->grid < 1) return GEMM_ERR_INVALID_ARG;
         return GEMM_OK;
     }
     if (p->path != GEMM_PATH_TENSOR) return GEMM_ERR_INVALID_ARG;

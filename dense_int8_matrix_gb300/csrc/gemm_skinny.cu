@@ -1,4 +1,5 @@
-// Skinny int8 GEMM (m <= 64): C = A x B where B (stored K-major as Bt,
+// Skinny int8 GEMM on CUDA cores (m <= 128, in launches of at most 64 rows;
+// used when the tensor-core skinny kernel does not apply): C = A x B where B (stored K-major as Bt,
 // n x k) is far larger than A, so the kernel's job is to stream Bt from HBM
 // once.  The patent CN114238853A (claim 4 S3) notes that such shapes are too
 // small to fill the chip with output tiles; here they get their own kernel.
@@ -116,7 +117,13 @@ __global__ void __launch_bounds__(kSkWarps * 32) skinny_bytes_kernel(const int8_
 cudaError_t launch_skinny_i8(const int8_t* A, const int8_t* Bt, int32_t* C, int64_t m, int64_t n, int64_t k,
                              int num_sms, cudaStream_t stream) {
     (void)num_sms;
-    if (m < 1 || m > 64) return cudaErrorInvalidValue;
+    if (m < 1 || m > 128) return cudaErrorInvalidValue;
+    if (m > 64) {
+        // rows 0..63, then the rest
+        const cudaError_t e = launch_skinny_i8(A, Bt, C, 64, n, k, num_sms, stream);
+        if (e != cudaSuccess) return e;
+        return launch_skinny_i8(A + 64 * k, Bt, C + 64 * n, m - 64, n, k, num_sms, stream);
+    }
     const unsigned grid = static_cast<unsigned>((n + kSkCols - 1) / kSkCols);
     const bool vec = (k % 16) == 0 &&
                      ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bt)) & 15u) == 0;

@@ -1,10 +1,10 @@
-// Skinny int8 GEMM on the tensor cores (m <= 64): C = A x B with B stored
+// Skinny int8 GEMM on the tensor cores (m <= 128): C = A x B with B stored
 // K-major as Bt (n x k).  Bt (n*k bytes) dwarfs A and C, so the kernel's job is
 // to stream Bt from HBM once, at full bandwidth; the patent CN114238853A
 // (claim 4 S3) calls such shapes too small to fill the chip with output tiles.
 //
 // Computed as C^T = Bt x A^T ("swap AB"): the MMA's M side is 128 rows of Bt,
-// its N side is m padded to NP in {16, 32, 64}, fp32 accumulation in TMEM,
+// its N side is m padded to NP in {16, 32, 64, 128}, fp32 accumulation in TMEM,
 // drained to exact int32 every 1024 K elements as in the large kernel.
 //
 // A pipeline stage is 256 K elements (four K steps of 64): every Bt row is
@@ -22,7 +22,8 @@
 //               warp of a group per TMEM lane quarter): each lane reads its
 //               Bt row (256 int8) from shared memory, releases the stage,
 //               widens the row to f16 in registers (exact) and writes it with
-//               tcgen05.st into one of three 128-column TMEM operand buffers.
+//               tcgen05.st into one of three 128-column TMEM operand buffers
+//               (two for NP = 128, whose accumulators take 256 columns).
 //               Shared memory carries only the int8 bytes, read once;
 //   warps 1, 3  one thread each issues the tcgen05.mma of alternate stages
 //               (A from TMEM, B = activations from shared memory): a small-N
@@ -51,13 +52,12 @@ constexpr int kSkKbPerStage = 4;                     // K steps of 64 per stage
 constexpr int kSkBtBox = 128 * 128;                  // one 128 B x 128-row box
 constexpr int kSkBtStage = 2 * kSkBtBox;             // 256 B x 128 rows
 constexpr int kSkGroups = 2;                         // widening groups (4 warps each)
-constexpr int kSkAbufs = 3;                          // TMEM operand buffers, 128 columns each
 // Barriers that two alternating warps (issuers or widening groups) would wait
 // on at alternate phases are kept apart instead: a parity wait can only tell
 // two neighbouring phases apart, so every barrier must have one waiter
-// sequence.  Operand-buffer barriers are indexed by stage mod 6 (buffer x
-// issuer), the Bt ring's "full" barriers by stage mod 2 x ring depth.
-constexpr int kSkAbufBars = 2 * kSkAbufs;
+// sequence.  Operand-buffer barriers are indexed by stage mod 2 x buffers
+// (buffer x issuer), the Bt ring's "full" barriers by stage mod 2 x ring
+// depth.
 constexpr int kSkEpiWarps = 8;
 constexpr int kSkWidenWarp0 = 4;
 constexpr int kSkEpiWarp0 = kSkWidenWarp0 + 4 * kSkGroups;
@@ -68,16 +68,20 @@ template <int NP>
 struct SkCfg {
     static constexpr int ACT_BOX = NP * 128;                   // f16 activation box: 64 K x NP rows
     static constexpr int ACT_STAGE = kSkKbPerStage * ACT_BOX;
+    // TMEM: ABUFS operand buffers of 128 columns and two NP-column accumulators.
+    static constexpr int ABUFS = NP >= 128 ? 2 : 3;
+    static constexpr int ABUF_BARS = 2 * ABUFS;
     // The activation ring must cover the MMA-to-refill latency (an L2 round
     // trip after the MMA two or more stages back completes); the Bt ring the
-    // HBM latency.
-    static constexpr int BT_STAGES = NP >= 32 ? 5 : 6;
+    // HBM latency.  NP = 128 activation stages are 64 KB: the Bt ring gets
+    // what is left.
+    static constexpr int BT_STAGES = NP >= 128 ? 3 : (NP >= 32 ? 5 : 6);
     static constexpr int ACT_STAGES = NP >= 64 ? 2 : 4;
-    static constexpr int TMEM_COLS = 512;                      // 3 x 128 operand + 2 x NP accumulator
+    static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = NP / 2;                    // columns per epilogue warp
     static constexpr size_t SMEM =
         static_cast<size_t>(BT_STAGES) * kSkBtStage + static_cast<size_t>(ACT_STAGES) * ACT_STAGE + 1024 + 1024;
-    static_assert(kSkAbufs * 128 + 2 * NP <= TMEM_COLS, "TMEM budget");
+    static_assert(ABUFS * 128 + 2 * NP <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -210,13 +214,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const uint32_t emptyB0 = fullB0 + 8u * kFullB;             // [BT_STAGES], stage n: n % BT_STAGES
     const uint32_t fullA0 = emptyB0 + 8u * Cfg::BT_STAGES;     // [ACT_STAGES]
     const uint32_t emptyA0 = fullA0 + 8u * Cfg::ACT_STAGES;    // [ACT_STAGES]
-    const uint32_t aready0 = emptyA0 + 8u * Cfg::ACT_STAGES;   // [kSkAbufBars], stage n: n % 6
-    const uint32_t afree0 = aready0 + 8u * kSkAbufBars;        // [kSkAbufBars], stage n: n % 6
-    const uint32_t accf0 = afree0 + 8u * kSkAbufBars;          // [2]
+    constexpr uint32_t kAbufs = Cfg::ABUFS, kAbufBars = Cfg::ABUF_BARS;
+    const uint32_t aready0 = emptyA0 + 8u * Cfg::ACT_STAGES;   // [ABUF_BARS], stage n: n % ABUF_BARS
+    const uint32_t afree0 = aready0 + 8u * kAbufBars;          // [ABUF_BARS], stage n: n % ABUF_BARS
+    const uint32_t accf0 = afree0 + 8u * kAbufBars;            // [2]
     const uint32_t acce0 = accf0 + 16u;                        // [2]
     const uint32_t done_bar = acce0 + 16u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(
-        ctrl + 8 * (kFullB + Cfg::BT_STAGES + 2 * Cfg::ACT_STAGES + 2 * kSkAbufBars + 5));
+        ctrl + 8 * (kFullB + Cfg::BT_STAGES + 2 * Cfg::ACT_STAGES + 2 * kAbufBars + 5));
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             mbar_init(fullA0 + 8u * s, 1);
             mbar_init(emptyA0 + 8u * s, 1);   // the MMA's commit
         }
-        for (int b = 0; b < kSkAbufBars; ++b) {
+        for (uint32_t b = 0; b < kAbufBars; ++b) {
             mbar_init(aready0 + 8u * b, 4);
             mbar_init(afree0 + 8u * b, 1);
         }
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tmem_acc = tmem_base + kSkAbufs * 128;   // two accumulators of NP columns
+    const uint32_t tmem_acc = tmem_base + kAbufs * 128;     // two accumulators of NP columns
 
     int64_t lo, hi;
     cta_range(p, lo, hi);
@@ -320,8 +325,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 const uint32_t buf = ch & 1u;
                 if (ok && (n & 1u) == g) {
                     const uint32_t sa = n % Cfg::ACT_STAGES, pha = (n / Cfg::ACT_STAGES) & 1u;
-                    const uint32_t b = n % kSkAbufs;
-                    const uint32_t rb = n % kSkAbufBars, rph = (n / kSkAbufBars) & 1u;
+                    const uint32_t b = n % kAbufs;
+                    const uint32_t rb = n % kAbufBars, rph = (n / kAbufBars) & 1u;
                     ok = (acc_ready || wait_bounded(acce0 + 8u * buf, (ch >> 1) & 1u, abort_flag, p.err,
                                                     kDevErrTimeoutMma)) &&
                          wait_bounded(fullA0 + 8u * sa, pha, abort_flag, p.err, kDevErrTimeoutMma) &&
@@ -376,15 +381,15 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         uint32_t n = g;
         for (int64_t i = lo + g; i < hi; i += kSkGroups, n += kSkGroups) {
             const uint32_t s = n % Cfg::BT_STAGES;
-            const uint32_t b = n % kSkAbufs;
+            const uint32_t b = n % kAbufs;
             int got = 1;
             if (lane == 0) {
                 got = wait_bounded(fullB0 + 8u * (n % kFullB), (n / kFullB) & 1u, abort_flag, p.err,
                                    kDevErrTimeoutEpilogue);
-                // buffer b last held stage n - 3: its MMAs must be complete
-                if (got && n >= static_cast<uint32_t>(kSkAbufs)) {
-                    const uint32_t pn = n - kSkAbufs;
-                    got = wait_bounded(afree0 + 8u * (pn % kSkAbufBars), (pn / kSkAbufBars) & 1u, abort_flag, p.err,
+                // buffer b last held stage n - ABUFS: its MMAs must be complete
+                if (got && n >= kAbufs) {
+                    const uint32_t pn = n - kAbufs;
+                    got = wait_bounded(afree0 + 8u * (pn % kAbufBars), (pn / kAbufBars) & 1u, abort_flag, p.err,
                                        kDevErrTimeoutEpilogue);
                 }
             }
@@ -412,7 +417,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(aready0 + 8u * (n % kSkAbufBars));
+            if (lane == 0) mbar_arrive(aready0 + 8u * (n % kAbufBars));
         }
     } else if (warp >= kSkEpiWarp0) {
         // ------------------------------------------------------- epilogue --
@@ -553,7 +558,7 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
 }  // namespace
 
 bool skinny_tc_supported(int64_t m, int64_t n, int64_t k, const void* A, const void* Bt) {
-    return m >= 1 && m <= 64 && (k % 16) == 0 && n <= 2147483647LL - 128 &&
+    return m >= 1 && m <= 128 && (k % 16) == 0 && n <= 2147483647LL - 128 &&
            ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bt)) & 15u) == 0;
 }
 
@@ -561,7 +566,8 @@ cudaError_t launch_skinny_tc(const int8_t* Bt, const uint16_t* A16, int32_t* C, 
                              int64_t k, int num_sms, cudaStream_t stream) {
     if (m <= 16) return launch_np<16>(Bt, A16, C, err, m, n, k, num_sms, stream);
     if (m <= 32) return launch_np<32>(Bt, A16, C, err, m, n, k, num_sms, stream);
-    return launch_np<64>(Bt, A16, C, err, m, n, k, num_sms, stream);
+    if (m <= 64) return launch_np<64>(Bt, A16, C, err, m, n, k, num_sms, stream);
+    return launch_np<128>(Bt, A16, C, err, m, n, k, num_sms, stream);
 }
 
 }  // namespace gemm

@@ -102,7 +102,7 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
         return GEMM_ERR_MISALIGNED;
     const bool skinny = p->path == GEMM_PATH_SKINNY;
     if (skinny) {
-        if (p->m > 64) return GEMM_ERR_INVALID_ARG;
+        if (p->m > 128) return GEMM_ERR_INVALID_ARG;
     } else {
         const bool pair_tile = p->bm == 256 && p->bn == 256 && (p->grid % 2) == 0;
         if (p->path != GEMM_PATH_TENSOR || (!pair_tile && p->bm != 64 && p->bm != 128) ||

@@ -20,7 +20,8 @@
 //   (unstated tie-break)      larger BM*BN, then larger BM
 //   claim 7                   every tile is a compiled template instance; the
 //                             plan names the one to launch
-// int8 problems with m <= 64 are routed to the skinny path first.
+// int8 problems with m <= 64, or m <= 128 and k % 16 == 0, are routed to the
+// skinny path first.
 #include <cstdint>
 
 #include "../../include/dense_int8_matrix.h"
@@ -95,8 +96,10 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
     p.k = k;
     p.n = n;
 
-    // Routing: a skinny int8 problem streams Bt once on CUDA cores.
-    if (dtype == GEMM_DTYPE_I8 && m <= 64) {
+    // Routing: a skinny int8 problem streams Bt once, widening it to f16 on
+    // chip; the tensor path would write and read an f16 copy of all of Bt.
+    // Up to 128 rows when the skinny tensor-core kernel applies (k % 16 == 0).
+    if (dtype == GEMM_DTYPE_I8 && (m <= 64 || (m <= 128 && k % 16 == 0))) {
         p.path = GEMM_PATH_SKINNY;
         p.bm = static_cast<int32_t>(m);
         p.bn = 32;

@@ -105,7 +105,8 @@ typedef struct gemm_plan {
 
 /*
  * Plan an int8 problem (m x k) x (k x n) for the current CUDA device.
- * Routing: m <= 64 -> skinny path (streams Bt once); otherwise the five
+ * Routing: m <= 64, or m <= 128 with k % 16 == 0 -> skinny path (streams Bt
+ * once, widening it on chip); otherwise the five
  * steps of CN114238853A claim 1 select a (BM, BN) tile.  Host-only apart from
  * one cached query of the device's SM count.
  * Errors: GEMM_ERR_INVALID_ARG (out == NULL, m/k/n outside [1, 2^31-1]),

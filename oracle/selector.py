@@ -35,7 +35,8 @@ Step 5 (claim 6): block_per_cu = min(registers of an SM // registers of a
     SM // TMEM columns of a CTA); Launch_kernel_times (waves) =
     ceil(Thread_Blocks / (SMs * block_per_cu)).  Keep the fewest waves.
 Tie-break (the pages are silent): larger BM*BN, then larger BM.
-Routing (before step 1): int8 problems with m <= 64 go to the skinny path.
+Routing (before step 1, the library's own rule): int8 problems with m <= 64,
+or m <= 128 when k is a multiple of 16, go to the skinny path.
 """
 
 from __future__ import annotations
@@ -138,7 +139,7 @@ def select(dtype: str, m: int, k: int, n: int, num_sms: int) -> dict:
     """Run the routing and the five steps; return the chosen configuration."""
     if dtype not in ("i8", "bf16"):
         raise ValueError(dtype)
-    if dtype == "i8" and m <= 64:
+    if dtype == "i8" and (m <= 64 or (m <= 128 and k % 16 == 0)):
         return {"path": "skinny"}
     # step 1
     cands = candidates()

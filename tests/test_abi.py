@@ -206,3 +206,9 @@ def test_skinny_plan_fields(lib):
     assert p.workspace_bytes == 0          # k % 8 == 0: bf16 operands are used in place
     p = B.gemm_plan_for_sms(B.GEMM_DTYPE_BF16, 64, 8190, 8192, 148)
     assert p.k_pitch == 8192 and p.workspace_bytes > 0
+    # 64 < m <= 128: skinny only when the tensor-core skinny kernel applies
+    assert B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 128, 8192, 8192, 148).path == B.GEMM_PATH_SKINNY
+    assert B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 65, 16, 100, 148).path == B.GEMM_PATH_SKINNY
+    assert B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 128, 8200, 8192, 148).path == B.GEMM_PATH_TENSOR
+    assert B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 129, 8192, 8192, 148).path == B.GEMM_PATH_TENSOR
+    assert B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 64, 8190, 8192, 148).path == B.GEMM_PATH_SKINNY

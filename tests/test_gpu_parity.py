@@ -330,6 +330,7 @@ def test_i8_tail_split_workloads_extreme():
 @pytest.mark.parametrize("m,k,n", [
     (1, 16, 1), (16, 64, 128), (17, 4112, 300), (33, 2048, 129), (64, 1040, 1000),
     (5, 20000, 640), (40, 8192, 8191), (64, 128, 40000),
+    (65, 1024, 1000), (100, 2064, 777), (128, 8192, 4096), (127, 16, 129),
 ])
 def test_i8_skinny_tensor_core_shapes(m, k, n):
     # k % 16 == 0: the tensor-core skinny kernel (stream-K over 128-row tiles,
@@ -339,7 +340,8 @@ def test_i8_skinny_tensor_core_shapes(m, k, n):
     G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
 
 
-@pytest.mark.parametrize("m,k,n", [(1, 8192, 8192), (16, 8192, 8192), (64, 8192, 8192), (5, 3328, 2000)])
+@pytest.mark.parametrize("m,k,n", [(1, 8192, 8192), (16, 8192, 8192), (64, 8192, 8192), (5, 3328, 2000),
+                                   (128, 8192, 8192), (90, 2048, 3000)])
 def test_i8_skinny_repeat_stress(m, k, n):
     # many back-to-back launches: the kernel's barrier protocol (two MMA
     # issuers and two widening groups sharing TMEM buffers and accumulators)
@@ -383,8 +385,9 @@ def test_i8_skinny_two_streams():
     assert B.gemm_device_error() == (B.GEMM_OK, 0)
 
 
-def test_i8_skinny_extremes():
-    m, k, n = 64, 16384, 1000
+@pytest.mark.parametrize("m", [64, 128])
+def test_i8_skinny_extremes(m):
+    k, n = 16384, 1000
     A = torch.full((m, k), -128, dtype=torch.int8)
     Bt = torch.full((n, k), -128, dtype=torch.int8)
     Bt[1::2] = 127

@@ -62,6 +62,8 @@ def test_noalloc_largest_problem_and_rejection():
     assert st == B.GEMM_ERR_INVALID_ARG
 
 
-def test_noalloc_skinny_plan():
-    out, ref = _both(16, 4096, 1000, 14)
+@pytest.mark.parametrize("m", [16, 100])
+def test_noalloc_skinny_plan(m):
+    # skinny plans run on CUDA cores here (no scratch); m > 64 in two launches
+    out, ref = _both(m, 4096, 1000, 14 + m)
     assert torch.equal(out, ref)
