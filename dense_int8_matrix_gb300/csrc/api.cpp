@@ -160,7 +160,7 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
             {
                 TraceScope t(GEMM_KERNEL_SKINNY, stream, sampled);
                 e = launch_stage_i8(static_cast<const int8_t*>(A), nullptr, static_cast<uint16_t*>(ws), nullptr, p->m, 0,
-                                    p->k, p->k, static_cast<int*>(C), p->m * p->n, ds->num_sms, stream);
+                                    p->k, p->k, static_cast<int*>(C), p->m * p->n, ds->err_word, ds->num_sms, stream);
                 if (e == cudaSuccess) {
                     trace_count(GEMM_KERNEL_STAGE);
                     e = launch_skinny_tc(static_cast<const int8_t*>(Bt), static_cast<const uint16_t*>(ws),
@@ -232,7 +232,7 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
             TraceScope t(GEMM_KERNEL_STAGE, stream, sampled);
             if (is_i8)
                 e = launch_stage_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), Ah, Bh, p->m, p->n,
-                                    p->k, p->k_pitch, flags, flag_count, ds->num_sms, stream);
+                                    p->k, p->k_pitch, flags, flag_count, ds->err_word, ds->num_sms, stream);
             else
                 e = launch_stage_b16(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(Bt), Ah, Bh, p->m,
                                      p->n, p->k, p->k_pitch, ds->num_sms, stream);

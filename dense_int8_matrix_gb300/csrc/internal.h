@@ -125,9 +125,11 @@ int tc_num_regs(int bm, int bn, bool int_out);
 // ---- operand staging (stage.cu) --------------------------------------------
 // int8 -> f16 (exact), row pitch k -> k_pitch, for A (m rows) and Bt (n rows).
 // Also zeroes `zero_count` ints at `zero` (the tail-split flags), if any.
+// `err`: device error word of the bulk-copy variant's bounded waits (nullptr:
+// that variant is not used).
 cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
-                            int64_t n, int64_t k, int64_t k_pitch, int* zero, int64_t zero_count, int num_sms,
-                            cudaStream_t stream);
+                            int64_t n, int64_t k, int64_t k_pitch, int* zero, int64_t zero_count, int* err,
+                            int num_sms, cudaStream_t stream);
 // 16-bit copy with row pitch k -> k_pitch (bf16 problems whose k is not a
 // multiple of 8).
 cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,

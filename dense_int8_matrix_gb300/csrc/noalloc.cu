@@ -127,7 +127,8 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;
     uint16_t* Ah = reinterpret_cast<uint16_t*>(d->scratch);
     uint16_t* Bh = reinterpret_cast<uint16_t*>(d->scratch + round256(p->m * p->k_pitch * 2));
-    if (launch_stage_i8(A, Bt, Ah, Bh, p->m, p->n, p->k, p->k_pitch, nullptr, 0, d->num_sms, stream) != cudaSuccess)
+    if (launch_stage_i8(A, Bt, Ah, Bh, p->m, p->n, p->k, p->k_pitch, nullptr, 0, d->err, d->num_sms, stream) !=
+        cudaSuccess)
         return GEMM_ERR_CUDA;
     TcLaunch L;
     L.A16 = Ah;
