@@ -159,8 +159,12 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
             cudaError_t e;
             {
                 TraceScope t(GEMM_KERNEL_SKINNY, stream, sampled);
+                StageZero z;   // all of C
+                z.C = static_cast<int32_t*>(C);
+                z.m = p->m;
+                z.n = p->n;
                 e = launch_stage_i8(static_cast<const int8_t*>(A), nullptr, static_cast<uint16_t*>(ws), nullptr, p->m, 0,
-                                    p->k, p->k, static_cast<int*>(C), p->m * p->n, ds->err_word, ds->num_sms, stream);
+                                    p->k, p->k, z, ds->err_word, ds->num_sms, stream);
                 if (e == cudaSuccess) {
                     trace_count(GEMM_KERNEL_STAGE);
                     e = launch_skinny_tc(static_cast<const int8_t*>(Bt), static_cast<const uint16_t*>(ws),
@@ -184,55 +188,30 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     const bool need_stage = is_i8 || (p->k_pitch != p->k);
     const int chunk_kb = p->chunk_k / kTcBK;
 
-    // Tail split, recomputed for the tile and grid actually launched.  One-SM
-    // tiles: only when every CTA of the grid can be resident at once (slices
-    // wait for slice 0 of their tile, which must be running).  Two-SM tile:
-    // over the pairs launch_tc2 runs; its slices never wait on one another.
-    const bool pair_tile = p->bm == 256;
+    // Tail split, recomputed for the tile and grid actually launched; the
+    // staging kernel zeroes C over the split tiles, into which every slice adds.
+    int64_t split_from = 0;
+    StageZero z;
+    const int split = tc_launch_split(static_cast<int32_t*>(C), p->m, p->n, p->k, p->bm, p->bn, p->grid, chunk_kb,
+                                      is_i8, ds->tc2_pairs, &split_from, &z);
     const int64_t tiles = ((p->m + p->bm - 1) / p->bm) * ((p->n + p->bn - 1) / p->bn);
-    int64_t split_from = tiles;
-    int split = 1;
-    {
-        const int64_t num_kb = (p->k + kTcBK - 1) / kTcBK;
-        const int64_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
-        if (pair_tile) {
-            split = tc_tail_split(tiles, tc2_pairs_for(p->grid, ds->tc2_pairs, tiles), nchunks, is_i8, &split_from);
-        } else {
-            const int64_t capacity = static_cast<int64_t>(ds->num_sms) * tc_blocks_per_sm(p->bm, p->bn);
-            if (p->grid <= capacity) split = tc_tail_split(tiles, p->grid, nchunks, is_i8, &split_from);
-        }
-        if (split > 1 && tiles - split_from > kTcSplitFlagTiles) split = 1;
-        if (split == 1) split_from = tiles;
-    }
-    // one-SM tiles: one flag per (split tile, epilogue warp); two-SM tile: one
-    // arrival counter per (split tile, CTA, epilogue warp) and the partial
-    // sums; flags and counters are zeroed by the staging kernel
-    const int64_t flag_count =
-        (tiles - split_from) * (pair_tile ? tc2_split_counters_per_tile() : kTcEpilogueWarps);
-    const int64_t partial_bytes = pair_tile ? (tiles - split_from) * tc2_split_ws_bytes_per_tile(split) : 0;
 
     void* ws = nullptr;
     const void* A16 = A;
     const void* B16 = Bt;
-    int* flags = nullptr;
-    void* partials = nullptr;
     if (need_stage) {
         const int64_t a_bytes = ((p->m * p->k_pitch * 2 + 255) / 256) * 256;
         const int64_t b_bytes = ((p->n * p->k_pitch * 2 + 255) / 256) * 256;
-        const int64_t f_bytes = ((flag_count * 4 + 255) / 256) * 256;
-        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes + f_bytes + partial_bytes), ds->pool,
-                                    stream) != cudaSuccess)
+        if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes), ds->pool, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
         uint16_t* Ah = static_cast<uint16_t*>(ws);
         uint16_t* Bh = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + a_bytes);
-        if (flag_count > 0) flags = reinterpret_cast<int*>(static_cast<char*>(ws) + a_bytes + b_bytes);
-        if (partial_bytes > 0) partials = static_cast<char*>(ws) + a_bytes + b_bytes + f_bytes;
         cudaError_t e;
         {
             TraceScope t(GEMM_KERNEL_STAGE, stream, sampled);
             if (is_i8)
                 e = launch_stage_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), Ah, Bh, p->m, p->n,
-                                    p->k, p->k_pitch, flags, flag_count, ds->err_word, ds->num_sms, stream);
+                                    p->k, p->k_pitch, z, ds->err_word, ds->num_sms, stream);
             else
                 e = launch_stage_b16(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(Bt), Ah, Bh, p->m,
                                      p->n, p->k, p->k_pitch, ds->num_sms, stream);
@@ -260,11 +239,9 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     L.grid = p->grid;
     L.chunk_kb = chunk_kb;
     L.int_out = is_i8;
-    L.split_k = flags ? split : 1;
-    L.split_from = flags ? split_from : tiles;
-    L.split_flags = flags;
-    L.epoch = 1;
-    L.split_ws = partials;
+    // int8 problems are always staged, so the split tiles' C is zero
+    L.split_k = need_stage ? split : 1;
+    L.split_from = need_stage ? split_from : tiles;
     cudaError_t e;
     {
         TraceScope t(GEMM_KERNEL_TC, stream, sampled);

@@ -66,23 +66,9 @@ struct TcParams {
     int chunk_kb;   // K steps per accumulator chunk
     int tiles_m, tiles_n, tiles;
     int units;      // split_from + (tiles - split_from) * split_k
-    int split_from; // tiles [split_from, tiles) run as split_k K slices each
+    int split_from; // tiles [split_from, tiles) run as split_k K slices each (C zeroed over them)
     int split_k;
-    uint32_t* split_flags;
-    uint32_t epoch;
 };
-
-constexpr int kBandM = 8;
-
-__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
-    const int per_band = kBandM * p.tiles_n;
-    const int band = t / per_band;
-    const int first_m = band * kBandM;
-    const int rows_in_band = min(kBandM, p.tiles_m - first_m);
-    const int local = t - band * per_band;
-    tm = first_m + local % rows_in_band;
-    tn = local / rows_in_band;
-}
 
 // A unit of work: one tile over the K steps [kb_lo, kb_hi).  Units below
 // split_from are whole tiles; above it, the slices of a split tile are
@@ -112,37 +98,8 @@ __device__ __forceinline__ Unit unit_at(int u, const TcParams& p) {
         x.kb_lo = (x.slice * nch / p.split_k) * p.chunk_kb;
         x.kb_hi = min(p.num_kb, ((x.slice + 1) * nch / p.split_k) * p.chunk_kb);
     }
-    tile_coords(t, p, x.tm, x.tn);
+    tc_tile_coords(t, p.tiles_m, p.tiles_n, x.tm, x.tn);
     return x;
-}
-
-__device__ __forceinline__ void st_release_gpu(uint32_t* addr, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* addr) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
-    return v;
-}
-
-// Wait (bounded) until *flag == epoch; on time-out raise the abort flag and
-// record the error.
-__device__ __forceinline__ bool wait_flag_bounded(const uint32_t* flag, uint32_t epoch, volatile uint32_t* abort_flag,
-                                                  int* err) {
-    if (ld_acquire_gpu(flag) == epoch) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1; it < kWaitIterCap; ++it) {
-        __nanosleep(64);
-        if (ld_acquire_gpu(flag) == epoch) return true;
-        if ((it & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
-        }
-    }
-    *abort_flag = 1u;
-    atomicCAS(err, 0, kDevErrTimeoutSplit);
-    return false;
 }
 
 template <int BM, int BN, bool INT_OUT, bool C_TMA>
@@ -192,9 +149,13 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // the epilogue writes C and the split flags only after the kernel before
-    // this one in the stream (programmatic dependent launch)
-    if (warp >= 4) pdl_wait();
+    // the epilogue writes C (zeroed over the split tiles by the staging
+    // kernel) only after the kernel before this one in the stream
+    // (programmatic dependent launch)
+    if (warp >= 4) {
+        pdl_wait();
+        fence_proxy_async_global();   // TMA reduce-adds below follow the zeroing
+    }
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer --
@@ -287,9 +248,8 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
         for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
             const Unit w = unit_at(u, p);
             const int tm = w.tm, tn = w.tn;
-            // slices 1.. of a split tile add into C after slice 0 has stored
-            const bool add_into = w.split_tile >= 0 && w.slice > 0;
-            uint32_t* flag = w.split_tile >= 0 ? p.split_flags + w.split_tile * kTcEpilogueWarps + e : nullptr;
+            // every slice of a split tile adds into C (zero over the tile)
+            const bool add_into = w.split_tile >= 0;
             const int64_t row = static_cast<int64_t>(tm) * BM + row_in_tile;
             const int64_t col0 = static_cast<int64_t>(tn) * BN + h * Cfg::HALF;
             // int8 problems: exact int32 running sums over the K chunks; bf16
@@ -312,16 +272,6 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                     break;
                 }
                 tc_fence_after();
-                if (last && add_into) {
-                    // this warp's region of C must hold slice 0's values first
-                    if (lane == 0) got = wait_flag_bounded(flag, p.epoch, abort_flag, p.err) ? 1 : 0;
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!got) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async_global();
-                }
                 const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * Cfg::HALF;
 #pragma unroll
                 for (int sl = 0; sl < Cfg::NSLICE; ++sl) {
@@ -402,18 +352,6 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce_bar0 + 8u * buf);
                 ++acc_iter;
-                if (last && w.split_tile >= 0 && w.slice == 0) {
-                    // publish: this warp's region of C holds slice 0's values
-                    if constexpr (C_TMA) {
-                        if (lane == 0) bulk_wait_all();
-                    }
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) {
-                        fence_proxy_async_global();
-                        st_release_gpu(flag, p.epoch);
-                    }
-                }
             }
         }
     }
@@ -516,8 +454,6 @@ cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     p.split_k = a.split_k > 1 ? a.split_k : 1;
     p.split_from = p.split_k > 1 ? static_cast<int>(a.split_from) : p.tiles;
     p.units = p.split_from + (p.tiles - p.split_from) * p.split_k;
-    p.split_flags = reinterpret_cast<uint32_t*>(a.split_flags);
-    p.epoch = a.epoch;
     auto kern = c_tma ? gemm_tc_kernel<BM, BN, INT_OUT, Cfg::TMA_STORE> : gemm_tc_kernel<BM, BN, INT_OUT, false>;
     cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;

@@ -26,11 +26,9 @@
 //
 // Tail split (int8 problems): when the last round of pairs is only partly
 // filled, the tiles of that round run as split_k K slices on otherwise idle
-// pairs.  Slices meet without waiting on one another: each epilogue warp
-// writes its exact int32 partial sums to a workspace slot and counts itself
-// on an atomic counter; the warp that arrives last adds the other slices'
-// partials and stores the tile.  No CTA ever waits on another, so the split
-// is correct whatever order or residency the pairs get.
+// pairs.  The staging kernel zeroes C over those tiles, and every slice adds
+// its exact int32 partial sums into C with a TMA reduce-add (atomics when C
+// cannot take TMA): no slice waits on another, whatever order the pairs run in.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -62,27 +60,9 @@ struct T2Params {
     int chunk_kb;
     int tiles_m, tiles_n, tiles;   // 256 x 256 tiles
     int units;                     // split_from + (tiles - split_from) * split_k
-    int split_from;                // tiles [split_from, tiles) run as split_k K slices
+    int split_from;                // tiles [split_from, tiles) run as split_k K slices (C zeroed over them)
     int split_k;
-    uint32_t* split_cnt;           // per (split tile, CTA of the pair, epilogue warp): arrivals, zeroed
-    int4* split_ws;                // per counter: split_k slots of 32 x 128 int32 partial sums
 };
-
-// Partial sums of one epilogue warp: 32 rows x 128 columns, stored as int4
-// with lane-fastest order so that every warp access is one coalesced 512 B.
-constexpr int kT2SlotInt4 = 32 * kT2Half2 / 4;
-
-constexpr int kBandM = 8;
-
-__device__ __forceinline__ void tile_coords2(int t, const T2Params& p, int& tm, int& tn) {
-    const int per_band = kBandM * p.tiles_n;
-    const int band = t / per_band;
-    const int first_m = band * kBandM;
-    const int rows_in_band = min(kBandM, p.tiles_m - first_m);
-    const int local = t - band * per_band;
-    tm = first_m + local % rows_in_band;
-    tn = local / rows_in_band;
-}
 
 // A unit of work: one tile over the K steps [kb_lo, kb_hi).  Units below
 // split_from are whole tiles; above it, the slices of a split tile are
@@ -111,7 +91,7 @@ __device__ __forceinline__ Unit2 unit_at2(int u, const T2Params& p) {
         x.kb_lo = (x.slice * nch / p.split_k) * p.chunk_kb;
         x.kb_hi = min(p.num_kb, ((x.slice + 1) * nch / p.split_k) * p.chunk_kb);
     }
-    tile_coords2(t, p, x.tm, x.tn);
+    tc_tile_coords(t, p.tiles_m, p.tiles_n, x.tm, x.tn);
     return x;
 }
 
@@ -181,30 +161,15 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* addr, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
-    return old;
-}
-
-// L2 load (bypassing L1) kept in program order, so that the fix-up reads one
-// 16-byte piece per lane at a time beside the 128 running sums
-__device__ __forceinline__ int4 ld_cg_v4(const int4* ptr) {
-    int4 v;
-    asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr)
-                 : "memory");
-    return v;
-}
-
-// Write one 32-column slice of this warp's 32 rows of C: each lane holds the
-// 32 values of its row.  With C_TMA, the lanes fill the warp's 128B-swizzled
-// 4 KiB staging buffer and one TMA store moves the 32 x 32 box (clipped at
-// the edges of C); otherwise each lane stores its row directly.
+// Write one 32-column slice of this warp's 32 rows of C, or add it into C
+// (`add`, the slices of a split tile): each lane holds the 32 values of its
+// row.  With C_TMA, the lanes fill the warp's 128B-swizzled 4 KiB staging
+// buffer and one TMA store (or reduce-add) moves the 32 x 32 box (clipped at
+// the edges of C); otherwise each lane stores (or atomically adds) its row.
 template <bool C_TMA>
 __device__ __forceinline__ void store_slice32(const CUtensorMap* tmC, const T2Params& p, const uint32_t (&r)[32],
-                                              uint32_t stg, int lane, int row, int ytop, int cs, bool c_vec) {
+                                              uint32_t stg, int lane, int row, int ytop, int cs, bool c_vec,
+                                              bool add) {
     if constexpr (C_TMA) {
         const uint32_t row_base = stg + lane * 128;
         if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
@@ -215,12 +180,19 @@ __device__ __forceinline__ void store_slice32(const CUtensorMap* tmC, const T2Pa
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(tmC, stg, cs, ytop);
+            if (add)
+                tma_reduce_add_2d(tmC, stg, cs, ytop);
+            else
+                tma_store_2d(tmC, stg, cs, ytop);
             bulk_commit();
         }
     } else if (row < p.m) {
         uint32_t* out = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row) * p.n + cs;
-        if (c_vec && cs + 32 <= p.n) {
+        if (add) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (cs + j < p.n) atomicAdd(out + j, r[j]);
+        } else if (c_vec && cs + 32 <= p.n) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4) *reinterpret_cast<uint4*>(out + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
         } else {
@@ -353,7 +325,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp >= 4) {
         // -------------------------------------------------------- epilogue --
-        pdl_wait();   // C and the split counters are written only after the kernel before
+        pdl_wait();   // C (zeroed over the split tiles by the staging kernel) only after the kernel before
+        fence_proxy_async_global();   // TMA reduce-adds below follow that zeroing
         const int e = warp - 4;
         const int q = warp & 3;
         const int h = e >> 2;
@@ -405,43 +378,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) mbar_arrive_cluster(acce_leader + 8u * buf);
                     ++acc_iter;
                     if (!last) continue;
-                    if (w.split_tile >= 0) {
-                        // this warp's 32 x 128 region of a split tile
-                        const int64_t region =
-                            (static_cast<int64_t>(w.split_tile) * 2 + rank) * kTcEpilogueWarps + e;
-                        int4* slots = p.split_ws + region * p.split_k * kT2SlotInt4;
-                        int4* mine = slots + w.slice * kT2SlotInt4;
-#pragma unroll
-                        for (int j = 0; j < kT2Half2 / 4; ++j)
-                            __stcg(mine + j * 32 + lane, make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
-                        __threadfence();
-                        __syncwarp();
-                        uint32_t before = 0;
-                        if (lane == 0) before = atomic_add_acq_rel_gpu(p.split_cnt + region, 1u);
-                        before = __shfl_sync(0xffffffffu, before, 0);
-                        if (before + 1u != static_cast<uint32_t>(p.split_k)) continue;   // another slice finishes the tile
-                        __threadfence();
-#pragma unroll
-                        for (int s = 0; s < kTcMaxSplit; ++s) {
-                            if (s >= p.split_k) break;
-                            if (s == w.slice) continue;
-                            const int4* other = slots + s * kT2SlotInt4;
-#pragma unroll
-                            for (int j = 0; j < kT2Half2 / 4; ++j) {
-                                const int4 x = ld_cg_v4(other + j * 32 + lane);
-                                acc[4 * j] += x.x;
-                                acc[4 * j + 1] += x.y;
-                                acc[4 * j + 2] += x.z;
-                                acc[4 * j + 3] += x.w;
-                            }
-                        }
-                    }
 #pragma unroll
                     for (int sl = 0; sl < kT2Half2 / 32; ++sl) {
                         uint32_t r[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = static_cast<uint32_t>(acc[sl * 32 + j]);
-                        store_slice32<C_TMA>(&tmC, p, r, stg, lane, row, ytop, col0 + sl * 32, c_vec);
+                        store_slice32<C_TMA>(&tmC, p, r, stg, lane, row, ytop, col0 + sl * 32, c_vec,
+                                             w.split_tile >= 0);
                     }
                 } else {
                     // fp32 results (one chunk): load and store 32 columns at a time
@@ -450,7 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         uint32_t r[32];
                         tmem_ld_32x32b_x32(tcol + sl * 32, r);
                         tmem_wait_ld();
-                        if (last) store_slice32<C_TMA>(&tmC, p, r, stg, lane, row, ytop, col0 + sl * 32, c_vec);
+                        if (last) store_slice32<C_TMA>(&tmC, p, r, stg, lane, row, ytop, col0 + sl * 32, c_vec, false);
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -551,12 +494,10 @@ cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
     const int pairs = tc2_pairs_for(a.grid, max_pairs, p.tiles);
     // the split was planned for this number of pairs; units only reorder the
     // work, so any pair count stays correct
-    const bool split = a.int_out && a.split_k > 1 && a.split_flags && a.split_ws && a.split_from < p.tiles;
+    const bool split = a.int_out && a.split_k > 1 && a.split_from < p.tiles;
     p.split_k = split ? a.split_k : 1;
     p.split_from = split ? static_cast<int>(a.split_from) : p.tiles;
     p.units = p.split_from + (p.tiles - p.split_from) * p.split_k;
-    p.split_cnt = split ? reinterpret_cast<uint32_t*>(a.split_flags) : nullptr;
-    p.split_ws = split ? static_cast<int4*>(a.split_ws) : nullptr;
     const void* kern = a.int_out ? (c_tma ? tc2_kernel_ptr<true, true>() : tc2_kernel_ptr<true, false>())
                                  : (c_tma ? tc2_kernel_ptr<false, true>() : tc2_kernel_ptr<false, false>());
     cudaError_t e = configure2(kern);

@@ -79,10 +79,23 @@ inline int tc_tail_split(int64_t tiles, int64_t grid, int64_t nchunks, bool int_
     return static_cast<int>(s);
 }
 
-// Flags of the tail split: one int per (split tile, epilogue warp), zeroed
-// before the launch and set to the launch's epoch once slice 0 of that tile
-// has stored that warp's region of C.
-constexpr int kTcSplitFlagTiles = 4096;
+// The slices of a split tile all add their int32 partial sums into C (TMA
+// reduce-add, or atomics), which the staging kernel has zeroed over those
+// tiles: no slice waits on another, whatever order the CTAs run in.
+
+// Order of the output tiles in both tensor kernels (and in the staging
+// kernel's zeroing of split tiles): bands of kTcBandM M-tiles, N fastest
+// inside a band, so CTAs running at the same time share A and Bt panels in L2.
+constexpr int kTcBandM = 8;
+__host__ __device__ inline void tc_tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+    const int per_band = kTcBandM * tiles_n;
+    const int band = t / per_band;
+    const int first_m = band * kTcBandM;
+    const int rows_in_band = tiles_m - first_m < kTcBandM ? tiles_m - first_m : kTcBandM;
+    const int local = t - band * per_band;
+    tm = first_m + local % rows_in_band;
+    tn = local / rows_in_band;
+}
 
 struct TcLaunch {
     const void* A16;      // m x k_pitch 16-bit operand (f16 for int8 problems, bf16 otherwise)
@@ -94,26 +107,17 @@ struct TcLaunch {
     int grid;
     int chunk_kb;         // k-blocks accumulated in TMEM before a drain
     bool int_out;         // true: int8 problem (f16 operands, int32 output)
-    int split_k;          // K slices of the tail tiles (1 = none)
+    int split_k;          // K slices of the tail tiles (1 = none); C is zero over those tiles
     int64_t split_from;   // first split tile
-    int* split_flags;     // one-SM tiles: (tiles - split_from) * kTcEpilogueWarps flags; two-SM tile:
-                          // (tiles - split_from) * tc2_split_counters_per_tile() counters; zeroed (device)
-    uint32_t epoch;       // launch epoch written to / awaited in split_flags (one-SM tiles)
-    void* split_ws = nullptr;   // two-SM tile: tc2_split_ws_bytes_per_tile(split_k) bytes per split tile
 };
 
 cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream);
 // Two-SM kernel (bm = bn = 256); max_pairs = co-resident clusters (0: unknown).
 cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream);
 int tc2_max_pairs();
-// Pairs launch_tc2 runs for a planned grid of 2 * pairs CTAs.
+// Pairs launch_tc2 runs for a planned grid of 2 * pairs CTAs (declared again
+// below, beside the tail split that uses it).
 int tc2_pairs_for(int grid, int max_pairs, int64_t tiles);
-// Tail split of the two-SM kernel: arrival counters and partial-sum bytes per
-// split tile (two CTAs x eight epilogue warps, each 32 x 128 int32 per slice).
-constexpr int tc2_split_counters_per_tile() { return 2 * kTcEpilogueWarps; }
-constexpr int64_t tc2_split_ws_bytes_per_tile(int split_k) {
-    return static_cast<int64_t>(split_k) * 2 * kTcEpilogueWarps * 32 * 128 * 4;
-}
 int tc2_num_regs(bool int_out);
 // block_per_cu of a tile as the planner counts it (registers, shared memory,
 // TMEM); the tail split is used only when the whole grid fits at once.
@@ -123,12 +127,51 @@ int tc_occupancy(int bm, int bn, bool int_out);
 int tc_num_regs(int bm, int bn, bool int_out);
 
 // ---- operand staging (stage.cu) --------------------------------------------
-// int8 -> f16 (exact), row pitch k -> k_pitch, for A (m rows) and Bt (n rows).
-// Also zeroes `zero_count` ints at `zero` (the tail-split flags), if any.
-// `err`: device error word of the bulk-copy variant's bounded waits (nullptr:
-// that variant is not used).
+// Int32 words of C that the staging kernel zeroes before a GEMM adds into
+// them: all of C (bm == 0; the skinny path), or the tiles [tile_from, tile_to)
+// of a bm x bn tiling in tc_tile_coords order (the tail split).
+struct StageZero {
+    int32_t* C = nullptr;   // nullptr: nothing to zero
+    int64_t m = 0, n = 0;
+    int bm = 0, bn = 0;
+    int tiles_m = 0, tiles_n = 0;
+    int tile_from = 0, tile_to = 0;
+};
+
+// Tail split of a tensor-path launch (tile bm x bn, persistent grid; for the
+// two-SM tile over the pairs launch_tc2 runs): returns S (1 = none) and sets
+// *split_from; `z` gets the split tiles of C for the staging kernel to zero.
+int tc2_pairs_for(int grid, int max_pairs, int64_t tiles);
+inline int tc_launch_split(int32_t* C, int64_t m, int64_t n, int64_t k, int bm, int bn, int grid, int chunk_kb,
+                           bool int_out, int tc2_pairs, int64_t* split_from, StageZero* z) {
+    const int tiles_m = static_cast<int>((m + bm - 1) / bm);
+    const int tiles_n = static_cast<int>((n + bn - 1) / bn);
+    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
+    const int64_t num_kb = (k + kTcBK - 1) / kTcBK;
+    const int64_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
+    const int64_t workers = bm == 256 ? tc2_pairs_for(grid, tc2_pairs, tiles) : grid;
+    const int split = tc_tail_split(tiles, workers, nchunks, int_out, split_from);
+    *z = StageZero{};
+    if (split > 1) {
+        z->C = C;
+        z->m = m;
+        z->n = n;
+        z->bm = bm;
+        z->bn = bn;
+        z->tiles_m = tiles_m;
+        z->tiles_n = tiles_n;
+        z->tile_from = static_cast<int>(*split_from);
+        z->tile_to = static_cast<int>(tiles);
+    } else {
+        *split_from = tiles;
+    }
+    return split;
+}
+// int8 -> f16 (exact), row pitch k -> k_pitch, for A (m rows) and Bt (n rows),
+// and the zeroing in `z`.  `err`: device error word of the bulk-copy
+// variant's bounded waits (nullptr: that variant is not used).
 cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
-                            int64_t n, int64_t k, int64_t k_pitch, int* zero, int64_t zero_count, int* err,
+                            int64_t n, int64_t k, int64_t k_pitch, const StageZero& z, int* err,
                             int num_sms, cudaStream_t stream);
 // 16-bit copy with row pitch k -> k_pitch (bf16 problems whose k is not a
 // multiple of 8).

@@ -127,8 +127,12 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;
     uint16_t* Ah = reinterpret_cast<uint16_t*>(d->scratch);
     uint16_t* Bh = reinterpret_cast<uint16_t*>(d->scratch + round256(p->m * p->k_pitch * 2));
-    if (launch_stage_i8(A, Bt, Ah, Bh, p->m, p->n, p->k, p->k_pitch, nullptr, 0, d->err, d->num_sms, stream) !=
-        cudaSuccess)
+    // tail split as in gemm_i8_run: the staging kernel zeroes C over the split tiles
+    int64_t split_from = 0;
+    StageZero z;
+    const int split = tc_launch_split(C, p->m, p->n, p->k, p->bm, p->bn, p->grid, p->chunk_k / kTcBK, true,
+                                      d->tc2_pairs, &split_from, &z);
+    if (launch_stage_i8(A, Bt, Ah, Bh, p->m, p->n, p->k, p->k_pitch, z, d->err, d->num_sms, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     TcLaunch L;
     L.A16 = Ah;
@@ -144,10 +148,8 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     L.grid = p->grid;
     L.chunk_kb = p->chunk_k / kTcBK;
     L.int_out = true;
-    L.split_k = 1;   // no tail split: its flags would need device memory
-    L.split_from = 0;
-    L.split_flags = nullptr;
-    L.epoch = 0;
+    L.split_k = split;
+    L.split_from = split_from;
     const cudaError_t e = p->bm == 256 ? launch_tc2(L, d->tc2_pairs, stream) : launch_tc(L, stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

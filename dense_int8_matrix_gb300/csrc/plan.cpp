@@ -213,22 +213,12 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
         p.workspace_bytes = (k % 8 == 0) ? 0 : round_up(m * k_pitch * 2, 256) + round_up(n * k_pitch * 2, 256);
     }
     // Beyond the five steps: split the last, partial wave along K (over CTA
-    // pairs for the two-SM tile), with the scratch the split needs.
+    // pairs for the two-SM tile).
     const int64_t nchunks = ceil_div(num_kb, p.chunk_k / kTcBK);
     int64_t split_from = tiles;
     const int64_t workers = is_pair(t) ? p.grid / 2 : p.grid;
     p.split_k = tc_tail_split(tiles, workers, nchunks, dtype == GEMM_DTYPE_I8, &split_from);
-    if (p.split_k > 1 && tiles - split_from > kTcSplitFlagTiles) {
-        p.split_k = 1;
-        split_from = tiles;
-    }
     p.split_from = static_cast<int32_t>(split_from);
-    if (p.split_k > 1) {
-        const int64_t split_tiles = tiles - split_from;
-        const int64_t words = split_tiles * (is_pair(t) ? tc2_split_counters_per_tile() : kTcEpilogueWarps);
-        p.workspace_bytes += round_up(words * 4, 256);
-        if (is_pair(t)) p.workspace_bytes += split_tiles * tc2_split_ws_bytes_per_tile(p.split_k);
-    }
     *out = p;
     return GEMM_OK;
 }

@@ -20,7 +20,6 @@ enum DeviceErrorCode : int {
     kDevErrTimeoutEpilogue = 3,   // epilogue waited too long for an accumulator
     kDevErrTimeoutTeardown = 4,   // teardown waited too long for in-flight copies / MMAs
     kDevErrTimeoutSelfTest = 5,   // the self-test's wait on a barrier nothing completes
-    kDevErrTimeoutSplit = 6,      // a split-tile slice waited too long for slice 0's stores
 };
 
 // One wait gives up after this many nanoseconds of %globaltimer time, or after

@@ -63,6 +63,44 @@ __device__ __forceinline__ void convert16(const uint4 v, uint4* d) {
 
 constexpr int kStageUnroll = 4;
 
+// Items of the zeroing work: 4 consecutive words of C (of all of C, or of a
+// row of a split tile), so that consecutive threads write consecutive 16-byte
+// pieces.
+__host__ __device__ inline int64_t zero_items(const StageZero& z) {
+    if (z.C == nullptr) return 0;
+    if (z.bm == 0) return (z.m * z.n + 3) / 4;
+    return static_cast<int64_t>(z.tile_to - z.tile_from) * z.bm * (z.bn / 4);
+}
+
+__device__ __forceinline__ void zero4(int32_t* p, int64_t avail, bool vec) {
+    if (vec && avail >= 4)
+        *reinterpret_cast<uint4*>(p) = make_uint4(0u, 0u, 0u, 0u);
+    else
+        for (int64_t j = 0; j < 4 && j < avail; ++j) p[j] = 0;
+}
+
+__device__ __forceinline__ void zero_work(const StageZero& z, int64_t i0, int64_t stride) {
+    const int64_t items = zero_items(z);
+    const bool vec = (z.n % 4) == 0 && (reinterpret_cast<uintptr_t>(z.C) & 15u) == 0;
+    if (z.bm == 0) {
+        const int64_t total = z.m * z.n;
+        for (int64_t i = i0; i < items; i += stride) zero4(z.C + 4 * i, total - 4 * i, vec);
+        return;
+    }
+    const int64_t q4 = z.bn / 4, per_tile = static_cast<int64_t>(z.bm) * q4;
+    for (int64_t i = i0; i < items; i += stride) {
+        const int t = z.tile_from + static_cast<int>(i / per_tile);
+        const int64_t rem = i % per_tile;
+        const int r = static_cast<int>(rem / q4);
+        const int64_t c = 4 * (rem % q4);
+        int tm, tn;
+        tc_tile_coords(t, z.tiles_m, z.tiles_n, tm, tn);
+        const int64_t row = static_cast<int64_t>(tm) * z.bm + r;
+        const int64_t col = static_cast<int64_t>(tn) * z.bn + c;
+        if (row < z.m && col < z.n) zero4(z.C + row * z.n + col, z.n - col, vec);
+    }
+}
+
 // ---- bulk-copy staging -------------------------------------------------
 constexpr int kBulkChunk = 16384;                  // int8 bytes per chunk
 constexpr int kBulkDepth = 4;                      // chunks in flight per CTA
@@ -106,8 +144,7 @@ __global__ void __launch_bounds__(kBulkThreads) stage_i8_bulk_kernel(const uint8
                                                                      const uint8_t* __restrict__ Bt,
                                                                      uint8_t* __restrict__ Ah, uint8_t* __restrict__ Bh,
                                                                      int64_t a_bytes, int64_t b_bytes,
-                                                                     int* __restrict__ zero, int64_t zero_count,
-                                                                     int* err) {
+                                                                     const StageZero z, int* err) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -118,9 +155,7 @@ __global__ void __launch_bounds__(kBulkThreads) stage_i8_bulk_kernel(const uint8
     __shared__ __align__(8) uint64_t full[kBulkDepth];
     __shared__ uint32_t abort_flag;
 
-    const int64_t stride_t = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_count; i += stride_t)
-        zero[i] = 0;
+    zero_work(z, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x, static_cast<int64_t>(gridDim.x) * blockDim.x);
 
     const int64_t na = (a_bytes + kBulkChunk - 1) / kBulkChunk;
     const int64_t nchunks = na + (b_bytes + kBulkChunk - 1) / kBulkChunk;
@@ -185,13 +220,11 @@ __global__ void __launch_bounds__(kBulkThreads) stage_i8_bulk_kernel(const uint8
 __global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restrict__ srcA,
                                                             const uint4* __restrict__ srcB, uint4* __restrict__ dstA,
                                                             uint4* __restrict__ dstB, int64_t itemsA,
-                                                            int64_t itemsB, int* __restrict__ zero,
-                                                            int64_t zero_count) {
+                                                            int64_t itemsB, const StageZero z) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
     const int64_t total = itemsA + itemsB;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_count; i += stride)
-        zero[i] = 0;
+    zero_work(z, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x, stride);
     for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
          i0 += stride * kStageUnroll) {
         uint4 v[kStageUnroll];
@@ -212,14 +245,12 @@ __global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restr
 __global__ void __launch_bounds__(256) stage_i8_rows_kernel(const int8_t* __restrict__ A,
                                                             const int8_t* __restrict__ Bt, __half* __restrict__ Ah,
                                                             __half* __restrict__ Bh, int64_t m, int64_t n, int64_t k,
-                                                            int64_t k_pitch, int* __restrict__ zero,
-                                                            int64_t zero_count) {
+                                                            int64_t k_pitch, const StageZero z) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
     const int64_t totalA = m * k;
     const int64_t total = totalA + n * k;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_count; i += stride)
-        zero[i] = 0;
+    zero_work(z, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x, stride);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
         const bool isA = i < totalA;
         const int64_t j = isA ? i : i - totalA;
@@ -258,7 +289,7 @@ int grid_for(int64_t items, int num_sms) {
 }  // namespace
 
 cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m, int64_t n,
-                            int64_t k, int64_t k_pitch, int* zero, int64_t zero_count, int* err, int num_sms,
+                            int64_t k, int64_t k_pitch, const StageZero& z, int* err, int num_sms,
                             cudaStream_t stream) {
     const bool aligned = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bt) |
                            reinterpret_cast<uintptr_t>(Ah) | reinterpret_cast<uintptr_t>(Bh)) &
@@ -271,16 +302,17 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
         const int grid = static_cast<int>(chunks < num_sms ? chunks : num_sms);
         stage_i8_bulk_kernel<<<grid, kBulkThreads, kBulkSmem, stream>>>(
             reinterpret_cast<const uint8_t*>(A), reinterpret_cast<const uint8_t*>(Bt), reinterpret_cast<uint8_t*>(Ah),
-            reinterpret_cast<uint8_t*>(Bh), m * k, n * k, zero, zero_count, err);
+            reinterpret_cast<uint8_t*>(Bh), m * k, n * k, z, err);
     } else if (k == k_pitch && (k % 16) == 0 && aligned) {
         const int64_t itemsA = m * k / 16, itemsB = n * k / 16;
-        const int64_t work = itemsA + itemsB > zero_count / 4 ? itemsA + itemsB : zero_count / 4;
+        const int64_t zi = zero_items(z);
+        const int64_t work = itemsA + itemsB > zi ? itemsA + itemsB : zi;
         stage_i8_flat_kernel<<<grid_for(work, num_sms), 256, 0, stream>>>(
             reinterpret_cast<const uint4*>(A), reinterpret_cast<const uint4*>(Bt), reinterpret_cast<uint4*>(Ah),
-            reinterpret_cast<uint4*>(Bh), itemsA, itemsB, zero, zero_count);
+            reinterpret_cast<uint4*>(Bh), itemsA, itemsB, z);
     } else {
         stage_i8_rows_kernel<<<grid_for((m + n) * k, num_sms), 256, 0, stream>>>(
-            A, Bt, reinterpret_cast<__half*>(Ah), reinterpret_cast<__half*>(Bh), m, n, k, k_pitch, zero, zero_count);
+            A, Bt, reinterpret_cast<__half*>(Ah), reinterpret_cast<__half*>(Bh), m, n, k, k_pitch, z);
     }
     return cudaGetLastError();
 }

@@ -70,14 +70,12 @@ enum {
  * Tail split (an addition to the patent's five steps, int8 only): when the
  * tiles do not fill a whole number of waves, the tiles of the last, partial
  * wave are split along K into split_k slices run by otherwise idle CTAs (CTA
- * pairs for the two-SM tile).  One-SM tiles: slice 0 stores its int32
- * partial sums; the other slices add theirs with TMA reduce-add once slice
- * 0's stores are complete.  Two-SM tile: every slice writes its partial sums
- * to scratch and counts itself on an atomic counter; the last to arrive adds
- * the others' partials and stores the tile (no slice waits on another).
- * Integer addition is exact and order-free, so the result is bit-identical
- * to the unsplit one.  gemm_*_run recomputes the split for the tile and grid
- * it actually launches.
+ * pairs for the two-SM tile).  The staging kernel zeroes C over those tiles
+ * and every slice adds its exact int32 partial sums into C (TMA reduce-add,
+ * or atomics when C cannot take TMA); no slice waits on another.  Integer
+ * addition is exact and order-free, so the result is bit-identical to the
+ * unsplit one.  gemm_*_run recomputes the split for the tile and grid it
+ * actually launches.
  */
 typedef struct gemm_plan {
     int32_t version;   /* GEMM_PLAN_VERSION */
@@ -96,8 +94,7 @@ typedef struct gemm_plan {
     int32_t fallback;    /* 1 if no tile filled the chip (claim 4 S3) */
     int32_t split_k;     /* K slices of each tile in the last, partial wave (1 = none) */
     double ratio;        /* compute-to-memory ratio of the tile (claim 5), flop per byte */
-    int64_t workspace_bytes; /* device scratch gemm_*_run takes from its pool: 16-bit operand
-                                copies and the tail split's flags / partial sums */
+    int64_t workspace_bytes; /* device scratch gemm_*_run takes from its pool (16-bit operand copies) */
     int32_t split_from;  /* tiles [split_from, tiles) are split into split_k K slices */
     int32_t reserved0;
     int64_t reserved[3];

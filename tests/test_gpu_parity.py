@@ -299,8 +299,8 @@ def test_bounded_wait_gives_up_and_reports():
     (13, 998, 2),     # n % 4 != 0: direct stores and atomic adds
 ])
 def test_i8_tail_split_exact(grid, n, split):
-    # int8 tiles of the last, partial wave split along K: slice 0 stores,
-    # the others add after it; the result must stay bit-exact
+    # int8 tiles of the last, partial wave split along K: the staging kernel
+    # zeroes C over them and every slice adds into it; bit-exact
     m, k = 1000, 4100
     A = workloads.random_i8((m, k), 41)
     Bt = workloads.random_i8((n, k), 42)
@@ -310,7 +310,7 @@ def test_i8_tail_split_exact(grid, n, split):
     assert min(grid // (tiles - full), 5, 8) == split
     C1 = G.gpu_i8(A, Bt, plan=p)
     G.assert_i8_exact(A, Bt, C1)
-    C2 = G.gpu_i8(A, Bt, plan=p)    # again: the flags start from zero every launch
+    C2 = G.gpu_i8(A, Bt, plan=p)    # again, into a poisoned C: the zeroing happens every launch
     assert torch.equal(C1, C2)
 
 
@@ -416,7 +416,7 @@ def test_i8_two_sm_tile_shapes(m, k, n, grid):
 ])
 def test_i8_two_sm_tail_split_exact(k, n, grid, split):
     # two-SM tiles of the last, partial round split along K over idle pairs:
-    # every slice writes its partial sums, the last to arrive adds and stores
+    # every slice adds into C, zeroed over those tiles by the staging kernel
     m = 1000
     A = workloads.random_i8((m, k), 51)
     Bt = workloads.random_i8((n, k), 52)
@@ -427,7 +427,7 @@ def test_i8_two_sm_tail_split_exact(k, n, grid, split):
     assert min(pairs // (tiles - tiles // pairs * pairs), nch, 8) == split
     C1 = G.gpu_i8(A, Bt, plan=p)
     G.assert_i8_exact(A, Bt, C1)
-    C2 = G.gpu_i8(A, Bt, plan=p)    # again: the counters start from zero every launch
+    C2 = G.gpu_i8(A, Bt, plan=p)    # again, into a poisoned C
     assert torch.equal(C1, C2)
     assert B.gemm_device_error() == (B.GEMM_OK, 0)
 
