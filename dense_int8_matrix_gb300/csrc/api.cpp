@@ -27,6 +27,8 @@ struct DeviceState {
     int* err_word = nullptr;
     int tc2_pairs = 0;                // co-resident CTA pairs of the two-SM kernel
     cudaMemPool_t pool = nullptr;
+    // side streams of the banded host entry point (created on first use)
+    cudaStream_t host_in = nullptr, host_gemm = nullptr, host_out = nullptr;
 };
 
 std::mutex g_mu;
@@ -258,6 +260,26 @@ gemm_status check_ptrs(const void* A, const void* Bt, const void* C) {
     return GEMM_OK;
 }
 
+// The end-to-end form is bound by the host link (about 200 GB/s each way on
+// GB300), so large tensor-path problems run in row bands on three streams:
+// Bt goes up first, then band i of A goes up while band i - 1 is multiplied
+// and band i - 2 of C comes down.
+constexpr int kHostMaxBands = 8;
+constexpr int64_t kHostBandMinRows = 512;
+constexpr int64_t kHostBandMinBytes = int64_t(16) << 20;   // host bytes moved
+
+gemm_status host_streams(DeviceState* ds) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (ds->host_out) return GEMM_OK;
+    cudaStream_t s[3] = {nullptr, nullptr, nullptr};
+    for (auto& x : s)
+        if (cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_CUDA;
+    ds->host_in = s[0];
+    ds->host_gemm = s[1];
+    ds->host_out = s[2];
+    return GEMM_OK;
+}
+
 gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const void* Bt, void* C, cudaStream_t stream) {
     gemm_status st = check_plan(p, dtype);
     if (st != GEMM_OK) return st;
@@ -271,18 +293,80 @@ gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const voi
     const size_t b_bytes = static_cast<size_t>(p->n * p->k) * es;
     const size_t c_bytes = static_cast<size_t>(p->m * p->n) * 4;
     const size_t a_al = (a_bytes + 255) / 256 * 256, b_al = (b_bytes + 255) / 256 * 256;
+    int64_t bands = 1;
+    if (p->path == GEMM_PATH_TENSOR && static_cast<int64_t>(a_bytes + b_bytes + c_bytes) >= kHostBandMinBytes) {
+        bands = p->m / kHostBandMinRows;
+        if (bands > kHostMaxBands) bands = kHostMaxBands;
+        if (bands < 1) bands = 1;
+    }
     void* buf = nullptr;
     if (cudaMallocFromPoolAsync(&buf, a_al + b_al + c_bytes, ds->pool, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     char* dA = static_cast<char*>(buf);
     char* dB = dA + a_al;
     char* dC = dB + b_al;
     st = GEMM_OK;
-    if (cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(dB, Bt, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        st = GEMM_ERR_CUDA;
-    if (st == GEMM_OK) st = run_device(p, dA, dB, dC, stream);
-    if (st == GEMM_OK && cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        st = GEMM_ERR_CUDA;
+    if (bands == 1) {
+        if (cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+            cudaMemcpyAsync(dB, Bt, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            st = GEMM_ERR_CUDA;
+        if (st == GEMM_OK) st = run_device(p, dA, dB, dC, stream);
+        if (st == GEMM_OK && cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+            st = GEMM_ERR_CUDA;
+    } else {
+        st = host_streams(ds);
+        cudaEvent_t ev[2 + 2 * kHostMaxBands + 2] = {};
+        const int nev = static_cast<int>(2 + 2 * bands + 2);
+        for (int i = 0; st == GEMM_OK && i < nev; ++i)
+            if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) st = GEMM_ERR_CUDA;
+        cudaEvent_t ev_start = ev[0], ev_b = ev[1], ev_gemm_done = ev[nev - 2], ev_out_done = ev[nev - 1];
+        cudaEvent_t* ev_a = ev + 2;
+        cudaEvent_t* ev_c = ev + 2 + bands;
+        const cudaStream_t s_in = ds->host_in, s_gemm = ds->host_gemm, s_out = ds->host_out;
+        // the side streams start after everything queued on `stream` (the
+        // pool allocation included)
+        if (st == GEMM_OK &&
+            (cudaEventRecord(ev_start, stream) != cudaSuccess || cudaStreamWaitEvent(s_in, ev_start, 0) != cudaSuccess ||
+             cudaStreamWaitEvent(s_gemm, ev_start, 0) != cudaSuccess ||
+             cudaStreamWaitEvent(s_out, ev_start, 0) != cudaSuccess))
+            st = GEMM_ERR_CUDA;
+        if (st == GEMM_OK && (cudaMemcpyAsync(dB, Bt, b_bytes, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+                              cudaEventRecord(ev_b, s_in) != cudaSuccess ||
+                              cudaStreamWaitEvent(s_gemm, ev_b, 0) != cudaSuccess))
+            st = GEMM_ERR_CUDA;
+        for (int64_t i = 0; i < bands; ++i) {
+            const int64_t r0 = p->m * i / bands, r1 = p->m * (i + 1) / bands;
+            const char* hA = static_cast<const char*>(A) + static_cast<size_t>(r0 * p->k) * es;
+            char* bA = dA + static_cast<size_t>(r0 * p->k) * es;
+            char* bC = dC + static_cast<size_t>(r0 * p->n) * 4;
+            char* hC = static_cast<char*>(C) + static_cast<size_t>(r0 * p->n) * 4;
+            gemm_plan bp;
+            if (st == GEMM_OK && make_plan(dtype, r1 - r0, p->k, p->n, ds->num_sms, &bp) != GEMM_OK) st = GEMM_ERR_CUDA;
+            if (st == GEMM_OK &&
+                (cudaMemcpyAsync(bA, hA, static_cast<size_t>((r1 - r0) * p->k) * es, cudaMemcpyHostToDevice, s_in) !=
+                     cudaSuccess ||
+                 cudaEventRecord(ev_a[i], s_in) != cudaSuccess || cudaStreamWaitEvent(s_gemm, ev_a[i], 0) != cudaSuccess))
+                st = GEMM_ERR_CUDA;
+            if (st == GEMM_OK) st = run_device(&bp, bA, dB, bC, s_gemm);
+            if (st == GEMM_OK &&
+                (cudaEventRecord(ev_c[i], s_gemm) != cudaSuccess || cudaStreamWaitEvent(s_out, ev_c[i], 0) != cudaSuccess ||
+                 cudaMemcpyAsync(hC, bC, static_cast<size_t>((r1 - r0) * p->n) * 4, cudaMemcpyDeviceToHost, s_out) !=
+                     cudaSuccess))
+                st = GEMM_ERR_CUDA;
+        }
+        // `stream` (and the pool's free below) waits for all three streams
+        if (ev_out_done != nullptr && ev_gemm_done != nullptr) {
+            cudaEventRecord(ev_gemm_done, s_gemm);
+            cudaEventRecord(ev_out_done, s_out);
+            cudaStreamWaitEvent(stream, ev_gemm_done, 0);
+            cudaStreamWaitEvent(stream, ev_out_done, 0);
+        }
+        cudaFreeAsync(buf, stream);
+        buf = nullptr;
+        if (cudaStreamSynchronize(stream) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
+        for (int i = 0; i < nev; ++i)
+            if (ev[i] != nullptr) cudaEventDestroy(ev[i]);
+        return st;
+    }
     cudaFreeAsync(buf, stream);
     if (cudaStreamSynchronize(stream) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
     return st;

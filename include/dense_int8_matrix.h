@@ -183,7 +183,11 @@ gemm_status gemm_i8_run_noalloc(const gemm_plan *plan, const int8_t *A, const in
  * End-to-end forms: A, Bt and C are HOST pointers (pinned or pageable).  The
  * call takes device buffers from the library's pool, copies A and Bt to the
  * device, runs the plan, copies C back and waits for `stream` to finish, so
- * C is ready when it returns.
+ * C is ready when it returns.  Large tensor-path problems (at least 16 MiB
+ * moved, at least 1024 rows) run in row bands of A and C on three library
+ * streams that follow `stream`, so the copies overlap the multiplies; each
+ * band is planned for its own shape, so an edited plan's tile applies only
+ * to unbanded calls.
  */
 gemm_status gemm_i8_run_host(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
                              void *stream);

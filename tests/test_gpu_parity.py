@@ -218,6 +218,29 @@ def test_host_entry_points():
     G.assert_bf16_close(Ab, Bb, Cb)
 
 
+@pytest.mark.parametrize("m,k,n,pinned", [(2048, 1024, 2048, True), (1500, 1040, 2100, False), (4096, 4096, 4096, True)])
+def test_host_entry_point_banded(m, k, n, pinned):
+    # at least 16 MiB moved and 1024 rows: row bands on three streams
+    A = workloads.random_i8((m, k), 27 + m)
+    Bt = workloads.random_i8((n, k), 28 + n)
+    C = torch.full((m, n), -7, dtype=torch.int32)
+    if pinned:
+        A, Bt, C = A.pin_memory(), Bt.pin_memory(), C.pin_memory()
+    B.gemm_i8_run_host(B.gemm_i8_plan(m, k, n), A, Bt, C)
+    G.assert_i8_exact(A, Bt, C)
+    B.gemm_i8_run_host(B.gemm_i8_plan(m, k, n), A, Bt, C, torch.cuda.Stream())   # on a side stream
+    G.assert_i8_exact(A, Bt, C)
+
+
+def test_host_entry_point_banded_bf16():
+    m, k, n = 1536, 512, 2304
+    A = workloads.random_bf16((m, k), 31)
+    Bt = workloads.random_bf16((n, k), 32)
+    C = torch.empty((m, n), dtype=torch.float32).pin_memory()
+    B.gemm_bf16_run_host(B.gemm_bf16_plan(m, k, n), A.pin_memory(), Bt.pin_memory(), C)
+    G.assert_bf16_close(A, Bt, C)
+
+
 def test_misaligned_device_pointers_rejected():
     lib = B.load()
     buf = torch.zeros(4096, dtype=torch.int8, device="cuda")
