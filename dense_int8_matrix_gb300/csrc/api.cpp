@@ -264,9 +264,12 @@ gemm_status check_ptrs(const void* A, const void* Bt, const void* C) {
 // GB300), so large tensor-path problems run in row bands on three streams:
 // Bt goes up first, then band i of A goes up while band i - 1 is multiplied
 // and band i - 2 of C comes down.
+// Band count: one band per 1024 rows and per 8 MiB of C, at most 8 (each band
+// restages Bt and gets a smaller, less efficient GEMM, so narrow-C problems,
+// whose time is the upload of A, stay whole).
 constexpr int kHostMaxBands = 8;
-constexpr int64_t kHostBandMinRows = 512;
-constexpr int64_t kHostBandMinBytes = int64_t(16) << 20;   // host bytes moved
+constexpr int64_t kHostBandMinRows = 1024;
+constexpr int64_t kHostBandCBytes = int64_t(8) << 20;
 
 gemm_status host_streams(DeviceState* ds) {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -294,8 +297,10 @@ gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const voi
     const size_t c_bytes = static_cast<size_t>(p->m * p->n) * 4;
     const size_t a_al = (a_bytes + 255) / 256 * 256, b_al = (b_bytes + 255) / 256 * 256;
     int64_t bands = 1;
-    if (p->path == GEMM_PATH_TENSOR && static_cast<int64_t>(a_bytes + b_bytes + c_bytes) >= kHostBandMinBytes) {
+    if (p->path == GEMM_PATH_TENSOR) {
         bands = p->m / kHostBandMinRows;
+        const int64_t by_c = static_cast<int64_t>(c_bytes) / kHostBandCBytes;
+        if (by_c < bands) bands = by_c;
         if (bands > kHostMaxBands) bands = kHostMaxBands;
         if (bands < 1) bands = 1;
     }

@@ -241,39 +241,56 @@ __global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restr
     }
 }
 
-// Any k: one element per item, rows re-pitched to k_pitch.
+// Any k or alignment: rows re-pitched to k_pitch (a multiple of 8); each item
+// is 8 elements of a row (byte loads, zero beyond k) and one 16-byte store.
 __global__ void __launch_bounds__(256) stage_i8_rows_kernel(const int8_t* __restrict__ A,
-                                                            const int8_t* __restrict__ Bt, __half* __restrict__ Ah,
-                                                            __half* __restrict__ Bh, int64_t m, int64_t n, int64_t k,
+                                                            const int8_t* __restrict__ Bt, uint4* __restrict__ Ah,
+                                                            uint4* __restrict__ Bh, int64_t m, int64_t n, int64_t k,
                                                             int64_t k_pitch, const StageZero z) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
-    const int64_t totalA = m * k;
-    const int64_t total = totalA + n * k;
+    const int64_t cpr = k_pitch / 8;   // 8-element pieces per staged row
+    const int64_t itemsA = m * cpr;
+    const int64_t total = itemsA + n * cpr;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     zero_work(z, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x, stride);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const bool isA = i < totalA;
-        const int64_t j = isA ? i : i - totalA;
-        const int64_t row = j / k, col = j - row * k;
-        const int8_t x = (isA ? A : Bt)[j];
-        (isA ? Ah : Bh)[row * k_pitch + col] = __short2half_rn(static_cast<short>(x));
+        const bool isA = i < itemsA;
+        const int64_t j = isA ? i : i - itemsA;
+        const int64_t row = j / cpr, c = j - row * cpr;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(isA ? A : Bt) + row * k + c * 8;
+        const int64_t left = k - c * 8;
+        uint32_t w[2] = {0u, 0u};   // zero bytes widen to 0 (the pad beyond k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e < left) w[e >> 2] |= static_cast<uint32_t>(src[e]) << (8 * (e & 3));
+        const uint32_t w0 = w[0] ^ 0x80808080u, w1 = w[1] ^ 0x80808080u;
+        (isA ? Ah : Bh)[row * cpr + c] = make_uint4(i8x2_to_f16x2(w0, 0x4140u), i8x2_to_f16x2(w0, 0x4342u),
+                                                    i8x2_to_f16x2(w1, 0x4140u), i8x2_to_f16x2(w1, 0x4342u));
     }
 }
 
-// 16-bit copy with re-pitched rows.
+// 16-bit copy with re-pitched rows: 8 elements per item (2-byte loads, zero
+// beyond k), one 16-byte store.
 __global__ void __launch_bounds__(256) stage_b16_rows_kernel(const uint16_t* __restrict__ A,
                                                              const uint16_t* __restrict__ Bt,
-                                                             uint16_t* __restrict__ Ah, uint16_t* __restrict__ Bh,
+                                                             uint4* __restrict__ Ah, uint4* __restrict__ Bh,
                                                              int64_t m, int64_t n, int64_t k, int64_t k_pitch) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
-    const int64_t totalA = m * k;
-    const int64_t total = totalA + n * k;
+    const int64_t cpr = k_pitch / 8;
+    const int64_t itemsA = m * cpr;
+    const int64_t total = itemsA + n * cpr;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const bool isA = i < totalA;
-        const int64_t j = isA ? i : i - totalA;
-        const int64_t row = j / k, col = j - row * k;
-        (isA ? Ah : Bh)[row * k_pitch + col] = (isA ? A : Bt)[j];
+        const bool isA = i < itemsA;
+        const int64_t j = isA ? i : i - itemsA;
+        const int64_t row = j / cpr, c = j - row * cpr;
+        const uint16_t* src = (isA ? A : Bt) + row * k + c * 8;
+        const int64_t left = k - c * 8;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e < left) w[e >> 1] |= static_cast<uint32_t>(src[e]) << (16 * (e & 1));
+        (isA ? Ah : Bh)[row * cpr + c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -311,15 +328,18 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
             reinterpret_cast<const uint4*>(A), reinterpret_cast<const uint4*>(Bt), reinterpret_cast<uint4*>(Ah),
             reinterpret_cast<uint4*>(Bh), itemsA, itemsB, z);
     } else {
-        stage_i8_rows_kernel<<<grid_for((m + n) * k, num_sms), 256, 0, stream>>>(
-            A, Bt, reinterpret_cast<__half*>(Ah), reinterpret_cast<__half*>(Bh), m, n, k, k_pitch, z);
+        const int64_t items = (m + n) * (k_pitch / 8);
+        const int64_t zi = zero_items(z);
+        stage_i8_rows_kernel<<<grid_for(items > zi ? items : zi, num_sms), 256, 0, stream>>>(
+            A, Bt, reinterpret_cast<uint4*>(Ah), reinterpret_cast<uint4*>(Bh), m, n, k, k_pitch, z);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
                              int64_t n, int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream) {
-    stage_b16_rows_kernel<<<grid_for((m + n) * k, num_sms), 256, 0, stream>>>(A, Bt, Ah, Bh, m, n, k, k_pitch);
+    stage_b16_rows_kernel<<<grid_for((m + n) * (k_pitch / 8), num_sms), 256, 0, stream>>>(
+        A, Bt, reinterpret_cast<uint4*>(Ah), reinterpret_cast<uint4*>(Bh), m, n, k, k_pitch);
     return cudaGetLastError();
 }
 

@@ -183,9 +183,10 @@ gemm_status gemm_i8_run_noalloc(const gemm_plan *plan, const int8_t *A, const in
  * End-to-end forms: A, Bt and C are HOST pointers (pinned or pageable).  The
  * call takes device buffers from the library's pool, copies A and Bt to the
  * device, runs the plan, copies C back and waits for `stream` to finish, so
- * C is ready when it returns.  Large tensor-path problems (at least 16 MiB
- * moved, at least 1024 rows) run in row bands of A and C on three library
- * streams that follow `stream`, so the copies overlap the multiplies; each
+ * C is ready when it returns.  Large tensor-path problems (at least 2048
+ * rows and 16 MiB of C) run in row bands of A and C (one per 1024 rows and per
+ * 8 MiB of C, at most 8) on three library streams that follow `stream`, so
+ * the copies overlap the multiplies; each
  * band is planned for its own shape, so an edited plan's tile applies only
  * to unbanded calls.
  */

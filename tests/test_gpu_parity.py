@@ -218,9 +218,9 @@ def test_host_entry_points():
     G.assert_bf16_close(Ab, Bb, Cb)
 
 
-@pytest.mark.parametrize("m,k,n,pinned", [(2048, 1024, 2048, True), (1500, 1040, 2100, False), (4096, 4096, 4096, True)])
+@pytest.mark.parametrize("m,k,n,pinned", [(2048, 1024, 2048, True), (3000, 1040, 2800, False), (4096, 4096, 4096, True)])
 def test_host_entry_point_banded(m, k, n, pinned):
-    # at least 16 MiB moved and 1024 rows: row bands on three streams
+    # at least 2048 rows and 16 MiB of C: row bands on three streams
     A = workloads.random_i8((m, k), 27 + m)
     Bt = workloads.random_i8((n, k), 28 + n)
     C = torch.full((m, n), -7, dtype=torch.int32)
@@ -233,7 +233,7 @@ def test_host_entry_point_banded(m, k, n, pinned):
 
 
 def test_host_entry_point_banded_bf16():
-    m, k, n = 1536, 512, 2304
+    m, k, n = 2304, 512, 2304
     A = workloads.random_bf16((m, k), 31)
     Bt = workloads.random_bf16((n, k), 32)
     C = torch.empty((m, n), dtype=torch.float32).pin_memory()
