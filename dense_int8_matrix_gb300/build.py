@@ -21,7 +21,7 @@ LIB_NAME = "libgemm_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v",
               "-I" + INCLUDE, "-I" + CSRC]
 
 

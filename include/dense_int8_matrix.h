@@ -35,6 +35,14 @@
 
 #include <stdint.h>
 
+/* Only the entry points below are exported; the library is built with
+ * hidden default visibility. */
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -109,16 +117,16 @@ typedef struct gemm_plan {
  * Errors: GEMM_ERR_INVALID_ARG (out == NULL, m/k/n outside [1, 2^31-1]),
  * GEMM_ERR_OVERFLOW_RISK (k > GEMM_I8_MAX_K), GEMM_ERR_CUDA (no device).
  */
-gemm_status gemm_i8_plan(int64_t m, int64_t k, int64_t n, gemm_plan *out);
+GEMM_API gemm_status gemm_i8_plan(int64_t m, int64_t k, int64_t n, gemm_plan *out);
 
 /* Plan a bf16 problem for the current device (always the tensor-core path). */
-gemm_status gemm_bf16_plan(int64_t m, int64_t k, int64_t n, gemm_plan *out);
+GEMM_API gemm_status gemm_bf16_plan(int64_t m, int64_t k, int64_t n, gemm_plan *out);
 
 /*
  * Pure host planner: the same selection for an explicit SM count, with no
  * CUDA call at all.  dtype is GEMM_DTYPE_*.  Same errors as the above.
  */
-gemm_status gemm_plan_for_sms(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t num_sms,
+GEMM_API gemm_status gemm_plan_for_sms(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t num_sms,
                               gemm_plan *out);
 
 /*
@@ -134,7 +142,7 @@ gemm_status gemm_plan_for_sms(int32_t dtype, int64_t m, int64_t k, int64_t n, in
  * GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_CUDA.  Nothing is launched when an
  * error is returned.
  */
-gemm_status gemm_i8_run(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
+GEMM_API gemm_status gemm_i8_run(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
                         void *stream);
 
 /*
@@ -143,7 +151,7 @@ gemm_status gemm_i8_run(const gemm_plan *plan, const int8_t *A, const int8_t *Bt
  * |C - exact| <= 1e-3 * sum_k |a*b| elementwise.  Same rules and errors as
  * gemm_i8_run.
  */
-gemm_status gemm_bf16_run(const gemm_plan *plan, const uint16_t *A, const uint16_t *Bt, float *C,
+GEMM_API gemm_status gemm_bf16_run(const gemm_plan *plan, const uint16_t *A, const uint16_t *Bt, float *C,
                           void *stream);
 
 /*
@@ -176,7 +184,7 @@ gemm_status gemm_bf16_run(const gemm_plan *plan, const uint16_t *A, const uint16
  *     which gemm_device_error does not read.
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES (64ll << 20)
-gemm_status gemm_i8_run_noalloc(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
+GEMM_API gemm_status gemm_i8_run_noalloc(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
                                 void *stream);
 
 /*
@@ -190,9 +198,9 @@ gemm_status gemm_i8_run_noalloc(const gemm_plan *plan, const int8_t *A, const in
  * band is planned for its own shape, so an edited plan's tile applies only
  * to unbanded calls.
  */
-gemm_status gemm_i8_run_host(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
+GEMM_API gemm_status gemm_i8_run_host(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
                              void *stream);
-gemm_status gemm_bf16_run_host(const gemm_plan *plan, const uint16_t *A, const uint16_t *Bt, float *C,
+GEMM_API gemm_status gemm_bf16_run_host(const gemm_plan *plan, const uint16_t *A, const uint16_t *Bt, float *C,
                                void *stream);
 
 /*
@@ -201,7 +209,7 @@ gemm_status gemm_bf16_run_host(const gemm_plan *plan, const uint16_t *A, const u
  * and the kernel returned early; *code gets the stage that gave up) or
  * GEMM_ERR_CUDA.  `code` may be NULL.
  */
-gemm_status gemm_device_error(void *stream, int32_t *code);
+GEMM_API gemm_status gemm_device_error(void *stream, int32_t *code);
 
 /*
  * Tracing.  While enabled, every kernel launch made by gemm_*_run is counted
@@ -218,12 +226,12 @@ gemm_status gemm_device_error(void *stream, int32_t *code);
  * ms of the timed units, the number of timed units, and the number of
  * launches counted; it then disables tracing.  every >= 1.
  */
-gemm_status gemm_trace_begin(int32_t capacity, int32_t every);
-gemm_status gemm_trace_collect(float *ms_per_kind, int32_t *timed_per_kind, int32_t *launches_per_kind);
+GEMM_API gemm_status gemm_trace_begin(int32_t capacity, int32_t every);
+GEMM_API gemm_status gemm_trace_collect(float *ms_per_kind, int32_t *timed_per_kind, int32_t *launches_per_kind);
 
 /* Registers per thread and CTAs per SM of the compiled tensor-core kernel for
  * a tile (-1 / 0 if no such kernel); needs a device. */
-gemm_status gemm_tc_kernel_info(int32_t bm, int32_t bn, int32_t dtype, int32_t *regs, int32_t *ctas_per_sm);
+GEMM_API gemm_status gemm_tc_kernel_info(int32_t bm, int32_t bn, int32_t dtype, int32_t *regs, int32_t *ctas_per_sm);
 
 /*
  * Failure-detection self-test.  Launches one CTA that waits on a barrier
@@ -233,10 +241,10 @@ gemm_status gemm_tc_kernel_info(int32_t bm, int32_t bn, int32_t dtype, int32_t *
  * returns GEMM_ERR_TIMEOUT with *code = 5, and the CUDA context stays usable.
  * Nothing faults, traps or hangs.
  */
-gemm_status gemm_selftest_wait_timeout(int32_t timeout_us, void *stream);
+GEMM_API gemm_status gemm_selftest_wait_timeout(int32_t timeout_us, void *stream);
 
 /* Human-readable name of a status. */
-const char *gemm_status_string(gemm_status s);
+GEMM_API const char *gemm_status_string(gemm_status s);
 
 #ifdef __cplusplus
 }

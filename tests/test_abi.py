@@ -45,6 +45,21 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_library_exports_nothing_else(lib):
+    """Internal C++ helpers stay hidden: the only defined text symbols in the
+    dynamic table are the header's entry points."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", build_mod.LIB_PATH], check=True,
+                         capture_output=True, text=True).stdout
+    text_syms = sorted(line.split()[-1] for line in out.splitlines()
+                       if len(line.split()) == 3 and line.split()[1] == "T")
+    assert text_syms == declared_functions()
+
+
 def test_plan_struct_layout(lib):
     p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 1000, 777, 3000, 148)
     assert ctypes.sizeof(B.gemm_plan) == 136
