@@ -277,4 +277,67 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_format, uint32_t M,
     return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// ------------------------------------------- TMEM stores, int8 widening --
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// Exact int8 -> f16 widening in registers (the arithmetic is explained in
+// stage.cu): two int8 of an (x ^ 0x80)-biased word -> one f16x2 word.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t biased, uint32_t selector) {
+    uint32_t packed = __byte_perm(biased, 0x64646464u, selector);
+    uint32_t out;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(packed), "r"(0x64806480u));
+    return out;
+}
+
+// 16 int8 (one 16-byte vector, K order) -> 8 f16x2 words, K order.
+__device__ __forceinline__ void widen16(const uint4 v, uint32_t* w) {
+    const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u;
+    const uint32_t x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;
+    w[0] = i8x2_to_f16x2(x0, 0x4140u);
+    w[1] = i8x2_to_f16x2(x0, 0x4342u);
+    w[2] = i8x2_to_f16x2(x1, 0x4140u);
+    w[3] = i8x2_to_f16x2(x1, 0x4342u);
+    w[4] = i8x2_to_f16x2(x2, 0x4140u);
+    w[5] = i8x2_to_f16x2(x2, 0x4342u);
+    w[6] = i8x2_to_f16x2(x3, 0x4140u);
+    w[7] = i8x2_to_f16x2(x3, 0x4342u);
+}
+
 }  // namespace gemm

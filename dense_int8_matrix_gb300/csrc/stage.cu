@@ -16,7 +16,6 @@
 // chunks out.  Measured on GB300 for the 4096^3 operands (32 MiB in, 64 MiB
 // out): 20.5 us, against 24.8 us for per-thread 16-byte loads and stores;
 // reading 32 MiB alone takes 8.2 us and writing 64 MiB alone 12.3 us.
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -27,16 +26,6 @@
 namespace gemm {
 
 namespace {
-
-__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t biased_word, uint32_t selector) {
-    // two bytes of the biased word become the low bytes of two f16 values
-    // whose high bytes are 0x64
-    const uint32_t packed = __byte_perm(biased_word, 0x64646464u, selector);
-    __half2 h = *reinterpret_cast<const __half2*>(&packed);
-    const __half2 offset = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-    h = __hsub2(h, offset);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     uint4 v;

@@ -461,3 +461,41 @@ def test_bf16_two_sm_tile_shapes(m, k, n):
     Bt = workloads.random_bf16((n, k), n + 29)
     p = forced_plan(B.GEMM_DTYPE_BF16, m, k, n, 256, 256, 8)
     G.assert_bf16_close(A, Bt, G.gpu_bf16(A, Bt, plan=p))
+
+
+# Two-SM (256 x 256) int8 tiles with k % 16 == 0: ragged m, n and k (a last
+# K chunk of 16 elements), persistent grids with many tiles per pair, a
+# single tile, and C that TMA cannot store (n % 4 != 0).
+@pytest.mark.parametrize("m,k,n,grid", [
+    (1000, 2064, 1000, 8),     # 4 x 4 tiles on 4 pairs; K = 1024 + 1024 + 16
+    (513, 1040, 4100, 6),      # 3 x 17 tiles on 3 pairs; last tile column 4 wide
+    (300, 128, 230, 2),        # two K steps; one tile column, 230 wide
+    (1024, 4096, 1002, 152),   # n % 4 != 0: direct stores of C
+    (256, 8192, 224, 2),       # exactly one tile, eight K chunks
+    (2048, 1024, 2560, 152),   # 80 tiles on 76 pairs; one K chunk, so no tail split
+])
+def test_i8_two_sm_k16_shapes(m, k, n, grid):
+    A = workloads.random_i8((m, k), m + 29)
+    Bt = workloads.random_i8((n, k), n + 31)
+    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, 256, 256, grid)
+    C1 = G.gpu_i8(A, Bt, plan=p)
+    G.assert_i8_exact(A, Bt, C1)
+    C2 = G.gpu_i8(A, Bt, plan=p)
+    assert torch.equal(C1, C2)
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
+@pytest.mark.parametrize("a,b", [(-128, -128), (-128, 127), (127, 127)])
+def test_i8_two_sm_chunk_extremes(a, b):
+    # on the two-SM tile, every 1024-element chunk sums to +-2^24 (or just
+    # below): exact only if each chunk is drained before fp32 would round
+    m, k, n = 512, 8192, 448
+    A = torch.full((m, k), a, dtype=torch.int8)
+    Bt = torch.full((n, k), b, dtype=torch.int8)
+    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, 256, 256, 4)
+    C = G.gpu_i8(A, Bt, plan=p)
+    assert torch.all(C == a * b * k)
+    Bt[1::2] = -b if b != -128 else 127
+    C = G.gpu_i8(A, Bt, plan=p)
+    assert torch.all(C[:, 0::2] == a * b * k)
+    assert torch.all(C[:, 1::2] == a * int(Bt[1, 0]) * k)
