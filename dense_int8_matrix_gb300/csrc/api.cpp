@@ -27,8 +27,11 @@ struct DeviceState {
     int* err_word = nullptr;
     int tc2_pairs = 0;                // co-resident CTA pairs of the two-SM kernel
     cudaMemPool_t pool = nullptr;
-    // side streams of the banded host entry point (created on first use)
-    cudaStream_t host_in = nullptr, host_gemm = nullptr, host_out = nullptr;
+    // the blocked host entry point: side streams and events (created on first
+    // use), taken by one call at a time
+    cudaStream_t host_in = nullptr, host_stage = nullptr, host_gemm = nullptr, host_out = nullptr;
+    std::vector<cudaEvent_t> host_events;
+    std::mutex host_mu;
 };
 
 std::mutex g_mu;
@@ -261,26 +264,218 @@ gemm_status check_ptrs(const void* A, const void* Bt, const void* C) {
 }
 
 // The end-to-end form is bound by the host link (about 200 GB/s each way on
-// GB300), so large tensor-path problems run in row bands on three streams:
-// Bt goes up first, then band i of A goes up while band i - 1 is multiplied
-// and band i - 2 of C comes down.
-// Band count: one band per 1024 rows and per 8 MiB of C, at most 8 (each band
-// restages Bt and gets a smaller, less efficient GEMM, so narrow-C problems,
-// whose time is the upload of A, stay whole).
-constexpr int kHostMaxBands = 8;
-constexpr int64_t kHostBandMinRows = 1024;
-constexpr int64_t kHostBandCBytes = int64_t(8) << 20;
+// GB300, 256 GB/s both ways at once), above all by copying C back, so large
+// tensor-path problems run as a pipeline on four streams: A is cut into row
+// bands and Bt into column bands (rows of Bt); the bands go up one by one,
+// each widened to f16 once on arrival, and every arrival completes a
+// rectangle of C (the new row band against the column bands already up, or
+// the new column band against the row bands already up), which one GEMM
+// writes into the device copy of C and one strided copy brings down while
+// later bands go up.  The bands go up in the order that completes the most
+// of C per byte, so the download, the longest leg, starts after a small part
+// of the input.  One GEMM per arrival (not per block): a GEMM takes at least
+// one tile's K loop, so fewer, larger launches keep the GEMM stream ahead of
+// the download.
+// Bands: at least 1024 rows of A or of Bt each, at most 8 per matrix; only
+// when C is at least 16 MiB and has at least 2048 rows (narrower problems
+// spend their time on the upload).
+constexpr int64_t kHostBandRows = 1024;
+constexpr int64_t kHostMaxBands = 8;
+constexpr int64_t kHostBlockedCBytes = int64_t(16) << 20;
 
-gemm_status host_streams(DeviceState* ds) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (ds->host_out) return GEMM_OK;
-    cudaStream_t s[3] = {nullptr, nullptr, nullptr};
-    for (auto& x : s)
-        if (cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_CUDA;
-    ds->host_in = s[0];
-    ds->host_gemm = s[1];
-    ds->host_out = s[2];
+gemm_status host_streams(DeviceState* ds, size_t events) {
+    if (!ds->host_out) {
+        cudaStream_t s[4] = {nullptr, nullptr, nullptr, nullptr};
+        for (auto& x : s)
+            if (cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_CUDA;
+        ds->host_in = s[0];
+        ds->host_stage = s[1];
+        ds->host_gemm = s[2];
+        ds->host_out = s[3];
+    }
+    while (ds->host_events.size() < events) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return GEMM_ERR_CUDA;
+        ds->host_events.push_back(e);
+    }
     return GEMM_OK;
+}
+
+// One rectangle of C on the tensor path, from operands already in device
+// memory (16-bit, row pitch k_pitch); C is m x n with row pitch ldc and is
+// written, not added to.  Rectangles run the two-SM 256 x 256 tile whatever
+// their size: a launch lasts at least one tile's K loop, and on rectangles
+// with fewer tiles than SMs the two-SM tile measured faster than the tiles
+// the selector picks to fill every SM.  An int8 rectangle with fewer tiles
+// than CTA pairs is split along K (whole 1024-element chunks) over the idle
+// pairs, every slice adding into C zeroed just before.
+gemm_status run_rect(DeviceState* ds, int32_t dtype, const void* A16, const void* B16, void* C, int64_t m, int64_t n,
+                     int64_t ldc, int64_t k, int64_t k_pitch, bool sampled, cudaStream_t stream) {
+    const bool is_i8 = dtype == GEMM_DTYPE_I8;
+    const int pairs = ds->tc2_pairs > 0 ? ds->tc2_pairs : 1;
+    const int64_t tiles = ((m + 255) / 256) * ((n + 255) / 256);
+    const int64_t num_kb = (k + kTcBK - 1) / kTcBK;
+    const int chunk_kb = is_i8 ? kI8ChunkK / kTcBK : static_cast<int>(num_kb);
+    int split = 1;
+    if (is_i8 && tiles < pairs) {
+        const int64_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
+        int64_t s = pairs / tiles;
+        if (s > nchunks) s = nchunks;
+        if (s > kTcMaxSplit) s = kTcMaxSplit;
+        split = static_cast<int>(s);
+    }
+    if (split > 1 && cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4, 0, static_cast<size_t>(n) * 4,
+                                       static_cast<size_t>(m), stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    TcLaunch L;
+    L.A16 = A16;
+    L.B16 = B16;
+    L.C = C;
+    L.err = ds->err_word;
+    L.m = m;
+    L.n = n;
+    L.k = k;
+    L.k_pitch = k_pitch;
+    L.bm = 256;
+    L.bn = 256;
+    L.grid = 2 * pairs;
+    L.chunk_kb = chunk_kb;
+    L.int_out = is_i8;
+    L.split_k = split;
+    L.split_from = split > 1 ? 0 : tiles;
+    L.ldc = ldc;
+    cudaError_t e;
+    {
+        TraceScope t(GEMM_KERNEL_TC, stream, sampled);
+        e = launch_tc2(L, ds->tc2_pairs, stream);
+    }
+    if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    trace_count(GEMM_KERNEL_TC);
+    return GEMM_OK;
+}
+
+gemm_status run_host_blocked(const gemm_plan* p, int32_t dtype, DeviceState* ds, const void* A, const void* Bt,
+                             void* C, cudaStream_t stream, int64_t RM, int64_t RN) {
+    const bool is_i8 = dtype == GEMM_DTYPE_I8;
+    const size_t es = is_i8 ? 1 : 2;
+    const int64_t m = p->m, n = p->n, k = p->k;
+    const int64_t kp = p->k_pitch;
+    const bool stage = is_i8 || kp != k;
+    auto al = [](int64_t b) { return static_cast<size_t>((b + 255) / 256 * 256); };
+    const size_t a_al = al(m * k * static_cast<int64_t>(es)), b_al = al(n * k * static_cast<int64_t>(es));
+    const size_t a16_al = stage ? al(m * kp * 2) : 0, b16_al = stage ? al(n * kp * 2) : 0;
+    const size_t c_bytes = static_cast<size_t>(m * n) * 4;
+
+    std::lock_guard<std::mutex> lock(ds->host_mu);
+    const size_t nev = 1 + 3 * static_cast<size_t>(RM + RN) + 4;
+    gemm_status st = host_streams(ds, nev);
+    if (st != GEMM_OK) return st;
+    void* buf = nullptr;
+    if (cudaMallocFromPoolAsync(&buf, a_al + b_al + a16_al + b16_al + c_bytes, ds->pool, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    char* dA = static_cast<char*>(buf);
+    char* dB = dA + a_al;
+    char* dA16 = dB + b_al;
+    char* dB16 = dA16 + a16_al;
+    char* dC = dB16 + b16_al;   // m x n, row pitch n, like the host's C
+    const cudaStream_t s_in = ds->host_in, s_stage = ds->host_stage, s_gemm = ds->host_gemm, s_out = ds->host_out;
+    cudaEvent_t* ev = ds->host_events.data();
+    cudaEvent_t ev_start = ev[0];
+    cudaEvent_t* ev_band = ev + 1;                 // [RM + RN]: per upload
+    cudaEvent_t* ev_staged = ev + 1 + RM + RN;     // [RM + RN]: per band widened
+    cudaEvent_t* ev_rect = ev + 1 + 2 * (RM + RN); // [RM + RN]: per rectangle of C
+    cudaEvent_t ev_in_done = ev[nev - 4], ev_stage_done = ev[nev - 3], ev_gemm_done = ev[nev - 2],
+                ev_out_done = ev[nev - 1];
+    const bool sampled = trace_sample_call();
+    auto edge = [](int64_t total, int64_t parts, int64_t i) { return total * i / parts; };
+
+    // the side streams start after everything queued on `stream` (the pool
+    // allocation included)
+    if (cudaEventRecord(ev_start, stream) != cudaSuccess || cudaStreamWaitEvent(s_in, ev_start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(s_stage, ev_start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(s_gemm, ev_start, 0) != cudaSuccess || cudaStreamWaitEvent(s_out, ev_start, 0) != cudaSuccess)
+        st = GEMM_ERR_CUDA;
+
+    int64_t ia = 0, ib = 0;   // bands of A and of Bt up so far
+    for (int64_t up = 0; st == GEMM_OK && up < RM + RN; ++up) {
+        // next band: A's row band 0, Bt's column band 0, then whichever
+        // completes more of C per byte uploaded (A on a tie)
+        bool take_a;
+        if (ia == 0 || ib == 0) {
+            take_a = ia == 0;
+        } else if (ia == RM || ib == RN) {
+            take_a = ia < RM;
+        } else {
+            // an A band of r rows (r * k bytes) completes r x (columns up
+            // so far) of C; a Bt band of r rows completes (rows up so far) x r
+            take_a = edge(n, RN, ib) >= edge(m, RM, ia);
+        }
+        const int64_t idx = take_a ? ia : ib;
+        const int64_t total = take_a ? m : n;
+        const int64_t parts = take_a ? RM : RN;
+        const int64_t r0 = edge(total, parts, idx), r1 = edge(total, parts, idx + 1);
+        const char* h = static_cast<const char*>(take_a ? A : Bt) + static_cast<size_t>(r0 * k) * es;
+        char* d = (take_a ? dA : dB) + static_cast<size_t>(r0 * k) * es;
+        if (cudaMemcpyAsync(d, h, static_cast<size_t>((r1 - r0) * k) * es, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+            cudaEventRecord(ev_band[up], s_in) != cudaSuccess ||
+            cudaStreamWaitEvent(stage ? s_stage : s_gemm, ev_band[up], 0) != cudaSuccess) {
+            st = GEMM_ERR_CUDA;
+            break;
+        }
+        // widening runs on its own stream, beside the multiplies of earlier
+        // rectangles
+        if (stage) {
+            char* d16 = (take_a ? dA16 : dB16) + static_cast<size_t>(r0 * kp) * 2;
+            cudaError_t e;
+            {
+                TraceScope t(GEMM_KERNEL_STAGE, s_stage, sampled);
+                e = is_i8 ? launch_stage_i8(reinterpret_cast<const int8_t*>(d), nullptr, reinterpret_cast<uint16_t*>(d16),
+                                            nullptr, r1 - r0, 0, k, kp, StageZero{}, ds->err_word, ds->num_sms, s_stage)
+                          : launch_stage_b16(reinterpret_cast<const uint16_t*>(d), nullptr,
+                                             reinterpret_cast<uint16_t*>(d16), nullptr, r1 - r0, 0, k, kp, ds->num_sms,
+                                             s_stage);
+            }
+            if (e != cudaSuccess || cudaEventRecord(ev_staged[up], s_stage) != cudaSuccess ||
+                cudaStreamWaitEvent(s_gemm, ev_staged[up], 0) != cudaSuccess) {
+                st = GEMM_ERR_CUDA;
+                break;
+            }
+            trace_count(GEMM_KERNEL_STAGE);
+        }
+        if (take_a)
+            ++ia;
+        else
+            ++ib;
+        // the rectangle this band completes
+        const int64_t m0 = take_a ? r0 : 0, m1 = take_a ? r1 : edge(m, RM, ia);
+        const int64_t n0 = take_a ? 0 : r0, n1 = take_a ? edge(n, RN, ib) : r1;
+        if (m1 <= m0 || n1 <= n0) continue;
+        const size_t a_off = stage ? static_cast<size_t>(m0 * kp) * 2 : static_cast<size_t>(m0 * k) * es;
+        const size_t b_off = stage ? static_cast<size_t>(n0 * kp) * 2 : static_cast<size_t>(n0 * k) * es;
+        const char* opA = (stage ? dA16 : dA) + a_off;
+        const char* opB = (stage ? dB16 : dB) + b_off;
+        const size_t c_off = static_cast<size_t>(m0 * n + n0) * 4;
+        st = run_rect(ds, dtype, opA, opB, dC + c_off, m1 - m0, n1 - n0, n, k, stage ? kp : k, sampled, s_gemm);
+        if (st == GEMM_OK &&
+            (cudaEventRecord(ev_rect[up], s_gemm) != cudaSuccess || cudaStreamWaitEvent(s_out, ev_rect[up], 0) != cudaSuccess ||
+             cudaMemcpy2DAsync(static_cast<char*>(C) + c_off, static_cast<size_t>(n) * 4, dC + c_off,
+                               static_cast<size_t>(n) * 4, static_cast<size_t>(n1 - n0) * 4,
+                               static_cast<size_t>(m1 - m0), cudaMemcpyDeviceToHost, s_out) != cudaSuccess))
+            st = GEMM_ERR_CUDA;
+    }
+    // `stream` (and the pool's free below) waits for all four streams,
+    // whatever was queued before an error
+    cudaEventRecord(ev_in_done, s_in);
+    cudaEventRecord(ev_stage_done, s_stage);
+    cudaEventRecord(ev_gemm_done, s_gemm);
+    cudaEventRecord(ev_out_done, s_out);
+    cudaStreamWaitEvent(stream, ev_in_done, 0);
+    cudaStreamWaitEvent(stream, ev_stage_done, 0);
+    cudaStreamWaitEvent(stream, ev_gemm_done, 0);
+    cudaStreamWaitEvent(stream, ev_out_done, 0);
+    cudaFreeAsync(buf, stream);
+    if (cudaStreamSynchronize(stream) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
+    return st;
 }
 
 gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const void* Bt, void* C, cudaStream_t stream) {
@@ -295,83 +490,26 @@ gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const voi
     const size_t a_bytes = static_cast<size_t>(p->m * p->k) * es;
     const size_t b_bytes = static_cast<size_t>(p->n * p->k) * es;
     const size_t c_bytes = static_cast<size_t>(p->m * p->n) * 4;
-    const size_t a_al = (a_bytes + 255) / 256 * 256, b_al = (b_bytes + 255) / 256 * 256;
-    int64_t bands = 1;
-    if (p->path == GEMM_PATH_TENSOR) {
-        bands = p->m / kHostBandMinRows;
-        const int64_t by_c = static_cast<int64_t>(c_bytes) / kHostBandCBytes;
-        if (by_c < bands) bands = by_c;
-        if (bands > kHostMaxBands) bands = kHostMaxBands;
-        if (bands < 1) bands = 1;
+    if (p->path == GEMM_PATH_TENSOR && static_cast<int64_t>(c_bytes) >= kHostBlockedCBytes &&
+        p->m >= 2 * kHostBandRows) {
+        int64_t RM = p->m / kHostBandRows, RN = p->n / kHostBandRows;
+        if (RM > kHostMaxBands) RM = kHostMaxBands;
+        if (RN > kHostMaxBands) RN = kHostMaxBands;
+        if (RN < 1) RN = 1;
+        return run_host_blocked(p, dtype, ds, A, Bt, C, stream, RM, RN);
     }
+    const size_t a_al = (a_bytes + 255) / 256 * 256, b_al = (b_bytes + 255) / 256 * 256;
     void* buf = nullptr;
     if (cudaMallocFromPoolAsync(&buf, a_al + b_al + c_bytes, ds->pool, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     char* dA = static_cast<char*>(buf);
     char* dB = dA + a_al;
     char* dC = dB + b_al;
-    st = GEMM_OK;
-    if (bands == 1) {
-        if (cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-            cudaMemcpyAsync(dB, Bt, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-            st = GEMM_ERR_CUDA;
-        if (st == GEMM_OK) st = run_device(p, dA, dB, dC, stream);
-        if (st == GEMM_OK && cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-            st = GEMM_ERR_CUDA;
-    } else {
-        st = host_streams(ds);
-        cudaEvent_t ev[2 + 2 * kHostMaxBands + 2] = {};
-        const int nev = static_cast<int>(2 + 2 * bands + 2);
-        for (int i = 0; st == GEMM_OK && i < nev; ++i)
-            if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) st = GEMM_ERR_CUDA;
-        cudaEvent_t ev_start = ev[0], ev_b = ev[1], ev_gemm_done = ev[nev - 2], ev_out_done = ev[nev - 1];
-        cudaEvent_t* ev_a = ev + 2;
-        cudaEvent_t* ev_c = ev + 2 + bands;
-        const cudaStream_t s_in = ds->host_in, s_gemm = ds->host_gemm, s_out = ds->host_out;
-        // the side streams start after everything queued on `stream` (the
-        // pool allocation included)
-        if (st == GEMM_OK &&
-            (cudaEventRecord(ev_start, stream) != cudaSuccess || cudaStreamWaitEvent(s_in, ev_start, 0) != cudaSuccess ||
-             cudaStreamWaitEvent(s_gemm, ev_start, 0) != cudaSuccess ||
-             cudaStreamWaitEvent(s_out, ev_start, 0) != cudaSuccess))
-            st = GEMM_ERR_CUDA;
-        if (st == GEMM_OK && (cudaMemcpyAsync(dB, Bt, b_bytes, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
-                              cudaEventRecord(ev_b, s_in) != cudaSuccess ||
-                              cudaStreamWaitEvent(s_gemm, ev_b, 0) != cudaSuccess))
-            st = GEMM_ERR_CUDA;
-        for (int64_t i = 0; i < bands; ++i) {
-            const int64_t r0 = p->m * i / bands, r1 = p->m * (i + 1) / bands;
-            const char* hA = static_cast<const char*>(A) + static_cast<size_t>(r0 * p->k) * es;
-            char* bA = dA + static_cast<size_t>(r0 * p->k) * es;
-            char* bC = dC + static_cast<size_t>(r0 * p->n) * 4;
-            char* hC = static_cast<char*>(C) + static_cast<size_t>(r0 * p->n) * 4;
-            gemm_plan bp;
-            if (st == GEMM_OK && make_plan(dtype, r1 - r0, p->k, p->n, ds->num_sms, &bp) != GEMM_OK) st = GEMM_ERR_CUDA;
-            if (st == GEMM_OK &&
-                (cudaMemcpyAsync(bA, hA, static_cast<size_t>((r1 - r0) * p->k) * es, cudaMemcpyHostToDevice, s_in) !=
-                     cudaSuccess ||
-                 cudaEventRecord(ev_a[i], s_in) != cudaSuccess || cudaStreamWaitEvent(s_gemm, ev_a[i], 0) != cudaSuccess))
-                st = GEMM_ERR_CUDA;
-            if (st == GEMM_OK) st = run_device(&bp, bA, dB, bC, s_gemm);
-            if (st == GEMM_OK &&
-                (cudaEventRecord(ev_c[i], s_gemm) != cudaSuccess || cudaStreamWaitEvent(s_out, ev_c[i], 0) != cudaSuccess ||
-                 cudaMemcpyAsync(hC, bC, static_cast<size_t>((r1 - r0) * p->n) * 4, cudaMemcpyDeviceToHost, s_out) !=
-                     cudaSuccess))
-                st = GEMM_ERR_CUDA;
-        }
-        // `stream` (and the pool's free below) waits for all three streams
-        if (ev_out_done != nullptr && ev_gemm_done != nullptr) {
-            cudaEventRecord(ev_gemm_done, s_gemm);
-            cudaEventRecord(ev_out_done, s_out);
-            cudaStreamWaitEvent(stream, ev_gemm_done, 0);
-            cudaStreamWaitEvent(stream, ev_out_done, 0);
-        }
-        cudaFreeAsync(buf, stream);
-        buf = nullptr;
-        if (cudaStreamSynchronize(stream) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
-        for (int i = 0; i < nev; ++i)
-            if (ev[i] != nullptr) cudaEventDestroy(ev[i]);
-        return st;
-    }
+    if (cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(dB, Bt, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        st = GEMM_ERR_CUDA;
+    if (st == GEMM_OK) st = run_device(p, dA, dB, dC, stream);
+    if (st == GEMM_OK && cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        st = GEMM_ERR_CUDA;
     cudaFreeAsync(buf, stream);
     if (cudaStreamSynchronize(stream) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_CUDA;
     return st;

@@ -62,6 +62,7 @@ struct TcParams {
     int* err;
     int c_tma;      // 1: write C with TMA stores (wide tiles, n % 4 == 0, C 16-byte aligned)
     int64_t m, n;
+    int64_t ldc;    // row pitch of C in elements
     int num_kb;     // ceil(k / 64)
     int chunk_kb;   // K steps per accumulator chunk
     int tiles_m, tiles_n, tiles;
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
         bool ok = true;
         const bool row_valid = (BM == 128) || (lane < 16);
         const int row_in_tile = (BM == 128) ? (q * 32 + lane) : (q * 16 + lane);
-        const bool c_vec = ((p.n & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+        const bool c_vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
             const Unit w = unit_at(u, p);
             const int tm = w.tm, tn = w.tn;
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                         }
                     } else {
                         if (row_valid && row < p.m) {
-                            uint32_t* out = static_cast<uint32_t*>(p.C) + row * p.n + cs;
+                            uint32_t* out = static_cast<uint32_t*>(p.C) + row * p.ldc + cs;
                             if (add_into) {
 #pragma unroll
                                 for (int j = 0; j < Cfg::SLICE; ++j)
@@ -412,13 +413,13 @@ cudaError_t configure_kernel(const void* kern, size_t smem) {
                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
 }
 
-// Tensor map of C (m x n, 4-byte elements) for TMA stores: box 32 x 32,
-// 128-byte swizzle.  Needs a 16-byte row pitch and base.
-bool encode_c_map(CUtensorMap* map, void* ptr, int64_t m, int64_t n) {
+// Tensor map of C (m x n, 4-byte elements, row pitch ldc elements) for TMA
+// stores: box 32 x 32, 128-byte swizzle.  Needs a 16-byte row pitch and base.
+bool encode_c_map(CUtensorMap* map, void* ptr, int64_t m, int64_t n, int64_t ldc) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(n) * 4u};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 4u};
     cuuint32_t box[2] = {32u, 32u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, ptr, dims, strides, box, estr,
@@ -436,8 +437,10 @@ cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     CUtensorMap mC;
     std::memset(&mC, 0, sizeof(mC));
     int c_tma = 0;
-    if (Cfg::TMA_STORE && (a.n % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0) {
-        if (!encode_c_map(&mC, a.C, a.m, a.n)) return cudaErrorInvalidValue;
+    const int64_t ldc = a.ldc > 0 ? a.ldc : a.n;
+    if (ldc < a.n) return cudaErrorInvalidValue;
+    if (Cfg::TMA_STORE && (ldc % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0) {
+        if (!encode_c_map(&mC, a.C, a.m, a.n, ldc)) return cudaErrorInvalidValue;
         c_tma = 1;
     }
     TcParams p;
@@ -446,6 +449,7 @@ cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     p.c_tma = c_tma;
     p.m = a.m;
     p.n = a.n;
+    p.ldc = ldc;
     p.num_kb = static_cast<int>((a.k + kTcBK - 1) / kTcBK);
     p.chunk_kb = a.chunk_kb;
     p.tiles_m = static_cast<int>((a.m + BM - 1) / BM);

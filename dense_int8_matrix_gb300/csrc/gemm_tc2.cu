@@ -56,6 +56,7 @@ struct T2Params {
     void* C;
     int* err;
     int64_t m, n;
+    int64_t ldc;                   // row pitch of C in elements
     int num_kb;
     int chunk_kb;
     int tiles_m, tiles_n, tiles;   // 256 x 256 tiles
@@ -187,7 +188,7 @@ __device__ __forceinline__ void store_slice32(const CUtensorMap* tmC, const T2Pa
             bulk_commit();
         }
     } else if (row < p.m) {
-        uint32_t* out = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row) * p.n + cs;
+        uint32_t* out = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc + cs;
         if (add) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t acc_iter = 0;
         bool ok = true;
         const int row_in_tile = q * 32 + lane;
-        const bool c_vec = ((p.n & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+        const bool c_vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         const uint32_t acce_leader = map_to_rank(acce_bar0, 0);
         const uint32_t stg = sEpi + e * kTcEpiStageBytes;
         for (int u = pair; ok && u < p.units; u += npairs) {
@@ -478,26 +479,29 @@ cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     if (!encode(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<void*>(a.B16), a.k, a.n, a.k_pitch * 2, kTcBK, kT2Half))
         return cudaErrorInvalidValue;
-    const bool c_tma = (a.n % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0;
-    if (c_tma && !encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.C, a.n, a.m, a.n * 4, 32, 32))
+    const int64_t ldc = a.ldc > 0 ? a.ldc : a.n;
+    if (ldc < a.n) return cudaErrorInvalidValue;
+    const bool c_tma = (ldc % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0;
+    if (c_tma && !encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.C, a.n, a.m, ldc * 4, 32, 32))
         return cudaErrorInvalidValue;
     T2Params p;
     p.C = a.C;
     p.err = a.err;
     p.m = a.m;
     p.n = a.n;
+    p.ldc = ldc;
     p.num_kb = static_cast<int>((a.k + kTcBK - 1) / kTcBK);
     p.chunk_kb = a.chunk_kb;
     p.tiles_m = static_cast<int>((a.m + 255) / 256);
     p.tiles_n = static_cast<int>((a.n + 255) / 256);
     p.tiles = p.tiles_m * p.tiles_n;
-    const int pairs = tc2_pairs_for(a.grid, max_pairs, p.tiles);
     // the split was planned for this number of pairs; units only reorder the
     // work, so any pair count stays correct
     const bool split = a.int_out && a.split_k > 1 && a.split_from < p.tiles;
     p.split_k = split ? a.split_k : 1;
     p.split_from = split ? static_cast<int>(a.split_from) : p.tiles;
     p.units = p.split_from + (p.tiles - p.split_from) * p.split_k;
+    const int pairs = tc2_pairs_for(a.grid, max_pairs, p.units);
     const void* kern = a.int_out ? (c_tma ? tc2_kernel_ptr<true, true>() : tc2_kernel_ptr<true, false>())
                                  : (c_tma ? tc2_kernel_ptr<false, true>() : tc2_kernel_ptr<false, false>());
     cudaError_t e = configure2(kern);

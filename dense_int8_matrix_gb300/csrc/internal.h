@@ -107,8 +107,9 @@ struct TcLaunch {
     int grid;
     int chunk_kb;         // k-blocks accumulated in TMEM before a drain
     bool int_out;         // true: int8 problem (f16 operands, int32 output)
-    int split_k;          // K slices of the tail tiles (1 = none); C is zero over those tiles
+    int split_k;          // K slices of the tail tiles (1 = none); C must be zero over those tiles
     int64_t split_from;   // first split tile
+    int64_t ldc = 0;      // row pitch of C in elements (0: n)
 };
 
 cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream);

@@ -220,7 +220,7 @@ def test_host_entry_points():
 
 @pytest.mark.parametrize("m,k,n,pinned", [(2048, 1024, 2048, True), (3000, 1040, 2800, False), (4096, 4096, 4096, True)])
 def test_host_entry_point_banded(m, k, n, pinned):
-    # at least 2048 rows and 16 MiB of C: row bands on three streams
+    # at least 2048 rows and 16 MiB of C: blocks of C on three streams
     A = workloads.random_i8((m, k), 27 + m)
     Bt = workloads.random_i8((n, k), 28 + n)
     C = torch.full((m, n), -7, dtype=torch.int32)
@@ -230,6 +230,31 @@ def test_host_entry_point_banded(m, k, n, pinned):
     G.assert_i8_exact(A, Bt, C)
     B.gemm_i8_run_host(B.gemm_i8_plan(m, k, n), A, Bt, C, torch.cuda.Stream())   # on a side stream
     G.assert_i8_exact(A, Bt, C)
+
+
+@pytest.mark.parametrize("m,k,n,pinned", [
+    (3000, 1040, 4500, True),    # 2 x 2 blocks, ragged bands (1500 rows; 2250 columns)
+    (4100, 1000, 8300, False),   # 4 x 4 blocks, k % 16 != 0 (re-pitched f16 rows), pageable
+    (2048, 4096, 4096, True),    # 2 x 2 blocks, four K chunks
+])
+def test_host_entry_point_blocked_shapes(m, k, n, pinned):
+    A = workloads.random_i8((m, k), 41 + m)
+    Bt = workloads.random_i8((n, k), 42 + n)
+    C = torch.full((m, n), -7, dtype=torch.int32)
+    if pinned:
+        A, Bt, C = A.pin_memory(), Bt.pin_memory(), C.pin_memory()
+    B.gemm_i8_run_host(B.gemm_i8_plan(m, k, n), A, Bt, C)
+    G.assert_i8_exact(A, Bt, C)
+
+
+def test_host_entry_point_blocked_bf16_repitched():
+    # bf16 with k % 8 != 0: each band is re-pitched once on the device
+    m, k, n = 2100, 1001, 4200
+    A = workloads.random_bf16((m, k), 43)
+    Bt = workloads.random_bf16((n, k), 44)
+    C = torch.full((m, n), float("nan"), dtype=torch.float32).pin_memory()
+    B.gemm_bf16_run_host(B.gemm_bf16_plan(m, k, n), A.pin_memory(), Bt.pin_memory(), C)
+    G.assert_bf16_close(A, Bt, C)
 
 
 def test_host_entry_point_banded_bf16():
