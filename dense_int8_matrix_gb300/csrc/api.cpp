@@ -277,11 +277,11 @@ gemm_status check_ptrs(const void* A, const void* Bt, const void* C) {
 // one tile's K loop, so fewer, larger launches keep the GEMM stream ahead of
 // the download.
 // Bands: at least 1024 rows of A or of Bt each, at most 8 per matrix; only
-// when C is at least 16 MiB and has at least 2048 rows (narrower problems
-// spend their time on the upload).
+// when C has at least 2048 rows and the copies move at least 32 MiB (a
+// narrow C still gains: its GEMMs hide behind the upload of A).
 constexpr int64_t kHostBandRows = 1024;
 constexpr int64_t kHostMaxBands = 8;
-constexpr int64_t kHostBlockedCBytes = int64_t(16) << 20;
+constexpr int64_t kHostPipelineBytes = int64_t(32) << 20;
 
 gemm_status host_streams(DeviceState* ds, size_t events) {
     if (!ds->host_out) {
@@ -490,7 +490,7 @@ gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const voi
     const size_t a_bytes = static_cast<size_t>(p->m * p->k) * es;
     const size_t b_bytes = static_cast<size_t>(p->n * p->k) * es;
     const size_t c_bytes = static_cast<size_t>(p->m * p->n) * 4;
-    if (p->path == GEMM_PATH_TENSOR && static_cast<int64_t>(c_bytes) >= kHostBlockedCBytes &&
+    if (p->path == GEMM_PATH_TENSOR && static_cast<int64_t>(a_bytes + b_bytes + c_bytes) >= kHostPipelineBytes &&
         p->m >= 2 * kHostBandRows) {
         int64_t RM = p->m / kHostBandRows, RN = p->n / kHostBandRows;
         if (RM > kHostMaxBands) RM = kHostMaxBands;

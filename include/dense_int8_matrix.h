@@ -192,11 +192,12 @@ GEMM_API gemm_status gemm_i8_run_noalloc(const gemm_plan *plan, const int8_t *A,
  * call takes device buffers from the library's pool, copies A and Bt to the
  * device, runs the plan, copies C back and waits for `stream` to finish, so
  * C is ready when it returns.  Large tensor-path problems (at least 2048
- * rows and 16 MiB of C) run as a pipeline on four library streams that
+ * rows of C, at least 32 MiB of A, Bt and C together) run as a pipeline on
+ * four library streams that
  * follow `stream`: A and Bt are cut into bands of at least 1024 rows (at most
  * 8 each), copied up one band at a time and widened once; each band's arrival
  * completes a rectangle of C, which is multiplied and copied down while later
- * bands go up.  Each rectangle is planned for its own shape, so an edited
+ * bands go up.  Rectangles run the two-SM 256 x 256 tile, so an edited
  * plan's tile applies only to calls that are not pipelined.  Calls on one
  * device take the pipeline one at a time.
  */

@@ -220,7 +220,7 @@ def test_host_entry_points():
 
 @pytest.mark.parametrize("m,k,n,pinned", [(2048, 1024, 2048, True), (3000, 1040, 2800, False), (4096, 4096, 4096, True)])
 def test_host_entry_point_banded(m, k, n, pinned):
-    # at least 2048 rows and 16 MiB of C: blocks of C on three streams
+    # at least 2048 rows and 32 MiB of copies: the band / rectangle pipeline
     A = workloads.random_i8((m, k), 27 + m)
     Bt = workloads.random_i8((n, k), 28 + n)
     C = torch.full((m, n), -7, dtype=torch.int32)
@@ -236,6 +236,7 @@ def test_host_entry_point_banded(m, k, n, pinned):
     (3000, 1040, 4500, True),    # 2 x 2 blocks, ragged bands (1500 rows; 2250 columns)
     (4100, 1000, 8300, False),   # 4 x 4 blocks, k % 16 != 0 (re-pitched f16 rows), pageable
     (2048, 4096, 4096, True),    # 2 x 2 blocks, four K chunks
+    (3000, 12288, 255, True),    # narrow C (n % 4 != 0): 2 x 1 bands, rectangles split 8 ways along K
 ])
 def test_host_entry_point_blocked_shapes(m, k, n, pinned):
     A = workloads.random_i8((m, k), 41 + m)
