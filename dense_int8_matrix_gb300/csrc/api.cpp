@@ -139,6 +139,7 @@ gemm_status check_plan(const gemm_plan* p, int32_t dtype) {
         (p->chunk_k % kTcBK) != 0)
         return GEMM_ERR_INVALID_ARG;
     if (dtype == GEMM_DTYPE_I8 && p->chunk_k > kI8ChunkK) return GEMM_ERR_INVALID_ARG;
+    if (p->split_k < 1 || p->split_k > kTcMaxSplit) return GEMM_ERR_INVALID_ARG;
     // bf16 problems accumulate the whole K in one TMEM chunk
     if (dtype == GEMM_DTYPE_BF16 && p->chunk_k < p->k) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
@@ -198,7 +199,7 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     int64_t split_from = 0;
     StageZero z;
     const int split = tc_launch_split(static_cast<int32_t*>(C), p->m, p->n, p->k, p->bm, p->bn, p->grid, chunk_kb,
-                                      is_i8, ds->tc2_pairs, &split_from, &z);
+                                      is_i8, ds->tc2_pairs, p->split_from == 0 ? p->split_k : 1, &split_from, &z);
     const int64_t tiles = ((p->m + p->bm - 1) / p->bm) * ((p->n + p->bn - 1) / p->bn);
 
     void* ws = nullptr;

@@ -74,7 +74,7 @@ struct TcParams {
 // A unit of work: one tile over the K steps [kb_lo, kb_hi).  Units below
 // split_from are whole tiles; above it, the slices of a split tile are
 // consecutive units (so they run in the same round on different CTAs), each
-// a run of whole accumulator chunks.
+// a run of whole K steps.
 struct Unit {
     int tm, tn, kb_lo, kb_hi;
     int split_tile;   // index among the split tiles, -1 if the tile is whole
@@ -95,9 +95,10 @@ __device__ __forceinline__ Unit unit_at(int u, const TcParams& p) {
         x.split_tile = v / p.split_k;
         x.slice = v - x.split_tile * p.split_k;
         t = p.split_from + x.split_tile;
-        const int nch = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
-        x.kb_lo = (x.slice * nch / p.split_k) * p.chunk_kb;
-        x.kb_hi = min(p.num_kb, ((x.slice + 1) * nch / p.split_k) * p.chunk_kb);
+        // K steps [kb_lo, kb_hi): accumulated in chunks of chunk_kb steps
+        // from kb_lo, so every fp32 chunk stays exact
+        x.kb_lo = x.slice * p.num_kb / p.split_k;
+        x.kb_hi = (x.slice + 1) * p.num_kb / p.split_k;
     }
     tc_tile_coords(t, p.tiles_m, p.tiles_n, x.tm, x.tn);
     return x;

@@ -139,19 +139,28 @@ struct StageZero {
     int tile_from = 0, tile_to = 0;
 };
 
-// Tail split of a tensor-path launch (tile bm x bn, persistent grid; for the
+// K split of a tensor-path launch (tile bm x bn, persistent grid; for the
 // two-SM tile over the pairs launch_tc2 runs): returns S (1 = none) and sets
 // *split_from; `z` gets the split tiles of C for the staging kernel to zero.
+// plan_split > 1 (int8): the plan splits every tile into that many K slices
+// (whole K steps); otherwise only the tail of a partial last round is split.
 int tc2_pairs_for(int grid, int max_pairs, int64_t tiles);
 inline int tc_launch_split(int32_t* C, int64_t m, int64_t n, int64_t k, int bm, int bn, int grid, int chunk_kb,
-                           bool int_out, int tc2_pairs, int64_t* split_from, StageZero* z) {
+                           bool int_out, int tc2_pairs, int plan_split, int64_t* split_from, StageZero* z) {
     const int tiles_m = static_cast<int>((m + bm - 1) / bm);
     const int tiles_n = static_cast<int>((n + bn - 1) / bn);
     const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
     const int64_t num_kb = (k + kTcBK - 1) / kTcBK;
     const int64_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
-    const int64_t workers = bm == 256 ? tc2_pairs_for(grid, tc2_pairs, tiles) : grid;
-    const int split = tc_tail_split(tiles, workers, nchunks, int_out, split_from);
+    int split;
+    if (int_out && plan_split > 1) {
+        split = plan_split < num_kb ? plan_split : static_cast<int>(num_kb);
+        if (split > kTcMaxSplit) split = kTcMaxSplit;
+        *split_from = 0;
+    } else {
+        const int64_t workers = bm == 256 ? tc2_pairs_for(grid, tc2_pairs, tiles) : grid;
+        split = tc_tail_split(tiles, workers, nchunks, int_out, split_from);
+    }
     *z = StageZero{};
     if (split > 1) {
         z->C = C;

@@ -127,11 +127,11 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;
     uint16_t* Ah = reinterpret_cast<uint16_t*>(d->scratch);
     uint16_t* Bh = reinterpret_cast<uint16_t*>(d->scratch + round256(p->m * p->k_pitch * 2));
-    // tail split as in gemm_i8_run: the staging kernel zeroes C over the split tiles
+    // K split as in gemm_i8_run: the staging kernel zeroes C over the split tiles
     int64_t split_from = 0;
     StageZero z;
     const int split = tc_launch_split(C, p->m, p->n, p->k, p->bm, p->bn, p->grid, p->chunk_k / kTcBK, true,
-                                      d->tc2_pairs, &split_from, &z);
+                                      d->tc2_pairs, p->split_from == 0 ? p->split_k : 1, &split_from, &z);
     if (launch_stage_i8(A, Bt, Ah, Bh, p->m, p->n, p->k, p->k_pitch, z, d->err, d->num_sms, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     TcLaunch L;

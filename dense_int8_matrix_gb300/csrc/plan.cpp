@@ -20,6 +20,10 @@
 //   (unstated tie-break)      larger BM*BN, then larger BM
 //   claim 7                   every tile is a compiled template instance; the
 //                             plan names the one to launch
+//   (after step 5, int8)      K split: small-MN, large-K problems whose choice
+//                             runs in one wave take the two-SM tile split
+//                             along K; otherwise the tail of a partial last
+//                             round is split
 // int8 problems with m <= 64, or m <= 128 and k % 16 == 0, are routed to the
 // skinny path first.
 #include <cstdint>
@@ -212,8 +216,35 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
         p.chunk_k = static_cast<int32_t>(num_kb * kTcBK > kMaxDim ? kMaxDim : num_kb * kTcBK);
         p.workspace_bytes = (k % 8 == 0) ? 0 : round_up(m * k_pitch * 2, 256) + round_up(n * k_pitch * 2, 256);
     }
-    // Beyond the five steps: split the last, partial wave along K (over CTA
-    // pairs for the two-SM tile).
+    // Beyond the five steps, int8 only (the slices of an int8 product add
+    // exactly):
+    // (i) small-MN, large-K: a one-wave choice gives way to the two-SM tile
+    //     split along K into S = min(pairs / its tiles, K steps / 16, 8)
+    //     slices when S >= 2 (every slice at least one 1024-element chunk,
+    //     all slices in one round);
+    if (dtype == GEMM_DTYPE_I8 && best_waves == 1) {
+        const Tile pair_tile{256, 256};
+        const int64_t pairs = num_sms / 2;
+        const int64_t t2 = out_tiles(pair_tile, m, n);
+        int64_t s = t2 > 0 ? pairs / t2 : 0;
+        if (s > num_kb / 16) s = num_kb / 16;
+        if (s > kTcMaxSplit) s = kTcMaxSplit;
+        if (s >= 2 && tile_fits(pair_tile) && t2 <= kMaxDim) {
+            p.bm = 256;
+            p.bn = 256;
+            p.tiles = static_cast<int32_t>(t2);
+            p.bpc = tile_bpc(pair_tile);
+            p.grid = static_cast<int32_t>(2 * (t2 * s < pairs ? t2 * s : pairs));
+            p.waves = static_cast<int32_t>(ceil_div(t2 * s, pairs));
+            p.ratio = tile_ratio(pair_tile);
+            p.split_k = static_cast<int32_t>(s);
+            p.split_from = 0;
+            *out = p;
+            return GEMM_OK;
+        }
+    }
+    // (ii) otherwise split the last, partial wave along K (over CTA pairs for
+    //     the two-SM tile).
     const int64_t nchunks = ceil_div(num_kb, p.chunk_k / kTcBK);
     int64_t split_from = tiles;
     const int64_t workers = is_pair(t) ? p.grid / 2 : p.grid;

@@ -37,6 +37,15 @@ Step 5 (claim 6): block_per_cu = min(registers of an SM // registers of a
 Tie-break (the pages are silent): larger BM*BN, then larger BM.
 Routing (before step 1, the library's own rule): int8 problems with m <= 64,
 or m <= 128 when k is a multiple of 16, go to the skinny path.
+K split (after step 5, the library's rule for small-MN, large-K problems,
+    where the pages' split-K technique applies: int8 only, since the slices
+    of an int8 product add exactly): when the five steps' choice runs in one
+    wave, the two-SM tile split into S slices along K replaces it if
+    S = min(floor(pairs / T2), floor(k_steps / 16), 8) >= 2, with pairs =
+    floor(SMs / 2), T2 = ceil(m/256) * ceil(n/256) and k_steps = ceil(k/64):
+    every slice keeps at least one 1024-element chunk, and the slices of all
+    tiles run at once.  The plan then has T2 tiles, block_per_cu 1 and
+    ceil(T2 * S / pairs) = 1 wave; "fallback" still records step 3.
 """
 
 from __future__ import annotations
@@ -161,7 +170,7 @@ def select(dtype: str, m: int, k: int, n: int, num_sms: int) -> dict:
     # tie-break
     cands.sort(key=lambda c: (c[0] * c[1], c[0]), reverse=True)
     bm, bn = cands[0]
-    return {
+    chosen = {
         "path": "tensor",
         "bm": bm,
         "bn": bn,
@@ -169,4 +178,28 @@ def select(dtype: str, m: int, k: int, n: int, num_sms: int) -> dict:
         "bpc": blocks_per_sm(bm, bn),
         "waves": best_w,
         "fallback": fallback,
+        "split": 1,
+    }
+    return k_split(dtype, m, k, n, num_sms, chosen)
+
+
+def k_split(dtype: str, m: int, k: int, n: int, num_sms: int, chosen: dict) -> dict:
+    """The K split after step 5 (see the module docstring)."""
+    if dtype != "i8" or chosen["waves"] != 1:
+        return chosen
+    pairs = num_sms // 2
+    t2 = tiles(m, n, 256, 256)
+    k_steps = math.ceil(k / BK_ELEMS)
+    s = min(pairs // t2, k_steps // 16, 8)
+    if s < 2:
+        return chosen
+    return {
+        "path": "tensor",
+        "bm": 256,
+        "bn": 256,
+        "tiles": t2,
+        "bpc": blocks_per_sm(256, 256),
+        "waves": math.ceil(t2 * s / pairs),
+        "fallback": chosen["fallback"],
+        "split": s,
     }

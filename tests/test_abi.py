@@ -72,13 +72,17 @@ def test_plan_struct_layout(lib):
 
 @pytest.mark.parametrize("ex", EXAMPLES, ids=lambda e: "%s-%dx%dx%d-%d" % e[:5])
 def test_planner_hand_examples(lib, ex):
-    d, m, k, n, sms, path, bm, bn, tiles, waves, fb = ex
+    d, m, k, n, sms, path, bm, bn, tiles, waves, fb, split = ex
     p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8 if d == "i8" else B.GEMM_DTYPE_BF16, m, k, n, sms)
     if path == "skinny":
         assert p.path == B.GEMM_PATH_SKINNY
         return
     assert p.path == B.GEMM_PATH_TENSOR
     assert (p.bm, p.bn, p.tiles, p.waves, bool(p.fallback)) == (bm, bn, tiles, waves, fb)
+    if split > 1:   # every tile split along K
+        assert (p.split_k, p.split_from) == (split, 0)
+    else:           # at most the tail of a partial last round
+        assert p.split_from > 0
 
 
 def test_planner_matches_selector_oracle_sweep(lib):
@@ -99,7 +103,10 @@ def test_planner_matches_selector_oracle_sweep(lib):
         got = (p.bm, p.bn, p.tiles, p.waves, p.bpc, bool(p.fallback))
         assert got == (want["bm"], want["bn"], want["tiles"], want["waves"], want["bpc"],
                        want["fallback"]), (d, m, k, n, sms)
-        if p.bm == 256:   # CTA pairs, one CTA per SM
+        if want["split"] > 1:   # every tile split: all slices in one round of pairs
+            assert (p.split_k, p.split_from) == (want["split"], 0)
+            assert p.grid == 2 * p.tiles * p.split_k <= 2 * (sms // 2)
+        elif p.bm == 256:       # CTA pairs, one CTA per SM
             assert p.grid == 2 * min(p.tiles, max(1, sms // 2))
         else:
             assert p.grid == min(p.tiles, sms * p.bpc)
@@ -148,6 +155,9 @@ def test_run_argument_errors_before_any_launch(lib):
     badb = B.gemm_plan_for_sms(B.GEMM_DTYPE_BF16, 256, 1000, 256, 148)
     badb.chunk_k = 512   # bf16 accumulates the whole K in one chunk
     assert lib.gemm_bf16_run(ctypes.byref(badb), 4096, 4096, 4096, s) == B.GEMM_ERR_INVALID_ARG
+    bad = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 256, 256, 256, 148)
+    bad.split_k = 9      # more K slices than the kernels take
+    assert lib.gemm_i8_run(ctypes.byref(bad), 4096, 4096, 4096, s) == B.GEMM_ERR_INVALID_ARG
     bad = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 256, 256, 256, 148)
     bad.k_pitch = 100
     assert lib.gemm_i8_run(ctypes.byref(bad), 4096, 4096, 4096, s) == B.GEMM_ERR_INVALID_ARG

@@ -525,3 +525,34 @@ def test_i8_two_sm_chunk_extremes(a, b):
     C = G.gpu_i8(A, Bt, plan=p)
     assert torch.all(C[:, 0::2] == a * b * k)
     assert torch.all(C[:, 1::2] == a * int(Bt[1, 0]) * k)
+
+
+# Small-MN, large-K int8 problems: the planner splits every two-SM tile along
+# K and every slice adds into C zeroed by the staging kernel.
+@pytest.mark.parametrize("m,k,n", [
+    (512, 8192, 512),      # 4 tiles x 8 slices
+    (1000, 4096, 300),     # 8 tiles x 4 slices; n % 4 != 0: slices add with atomics
+    (200, 4096, 4096),     # 16 tiles x 4 slices, one ragged tile row
+    (700, 3000, 900),      # k % 16 != 0 (re-pitched rows); 12 tiles x 2 slices of 23-24 K steps
+])
+def test_i8_k_split_plans_exact(m, k, n):
+    p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, m, k, n, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert p.bm == 256 and p.split_k >= 2 and p.split_from == 0
+    A = workloads.random_i8((m, k), m + 61)
+    Bt = workloads.random_i8((n, k), n + 62)
+    C1 = G.gpu_i8(A, Bt, plan=p)
+    G.assert_i8_exact(A, Bt, C1)
+    C2 = G.gpu_i8(A, Bt, plan=p)   # again, into a poisoned C
+    assert torch.equal(C1, C2)
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
+def test_i8_k_split_extremes_exact():
+    # 8 slices of 8192 K elements each, every chunk at +2^24: C = 2^30
+    m, k, n = 300, 65536, 300
+    p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, m, k, n, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert p.split_k == 8 and p.split_from == 0
+    A = torch.full((m, k), -128, dtype=torch.int8)
+    Bt = torch.full((n, k), -128, dtype=torch.int8)
+    C = G.gpu_i8(A, Bt, plan=p)
+    assert torch.all(C == 16384 * k)

@@ -1,5 +1,6 @@
 """Pins for the selector oracle: hand-worked examples of the patent's five
-steps (tests/golden/selector_examples.txt, derivations in its header)."""
+steps and of the K split after them (tests/golden/selector_examples.txt,
+derivations in its header)."""
 
 import os
 
@@ -17,9 +18,9 @@ def load_examples():
             line = line.strip()
             if not line or line.startswith("#"):
                 continue
-            d, m, k, n, sms, path, bm, bn, tiles, waves, fb = line.split()
+            d, m, k, n, sms, path, bm, bn, tiles, waves, fb, split = line.split()
             rows.append((d, int(m), int(k), int(n), int(sms), path, int(bm), int(bn),
-                         int(tiles), int(waves), bool(int(fb))))
+                         int(tiles), int(waves), bool(int(fb)), int(split)))
     return rows
 
 
@@ -28,7 +29,7 @@ EXAMPLES = load_examples()
 
 @pytest.mark.parametrize("ex", EXAMPLES, ids=lambda e: "%s-%dx%dx%d-%d" % e[:5])
 def test_selector_oracle_hand_examples(ex):
-    d, m, k, n, sms, path, bm, bn, tiles, waves, fb = ex
+    d, m, k, n, sms, path, bm, bn, tiles, waves, fb, split = ex
     got = selector.select(d, m, k, n, sms)
     assert got["path"] == path
     if path == "tensor":
@@ -36,6 +37,7 @@ def test_selector_oracle_hand_examples(ex):
         assert got["tiles"] == tiles
         assert got["waves"] == waves
         assert got["fallback"] == fb
+        assert got["split"] == split
 
 
 def test_selector_ratio_closed_form():
@@ -50,3 +52,16 @@ def test_selector_ratio_closed_form():
 def test_every_candidate_fits():
     assert all(selector.fits(*c) for c in selector.candidates())
     assert len(selector.candidates()) == 9
+
+
+def test_k_split_only_for_int8_one_wave_long_k():
+    # the K split never applies to bf16, to multi-wave choices, or when a
+    # slice would hold fewer than 16 K steps
+    assert selector.select("bf16", 1024, 16384, 1024, 148)["split"] == 1
+    assert selector.select("i8", 4096, 16384, 4096, 148)["split"] == 1
+    assert selector.select("i8", 512, 1023, 512, 148)["split"] == 1    # 15 K steps
+    assert selector.select("i8", 512, 2048, 512, 148)["split"] == 2    # 32 K steps
+    # the slices of all tiles fit one round of pairs
+    for shape in [(512, 8192, 512), (4097, 16384, 255), (1024, 16384, 1024), (300, 65536, 300)]:
+        got = selector.select("i8", *shape, 148)
+        assert got["split"] >= 2 and got["tiles"] * got["split"] <= 74 and got["waves"] == 1
