@@ -67,3 +67,12 @@ def test_noalloc_skinny_plan(m):
     # skinny plans run on CUDA cores here (no scratch); m > 64 in two launches
     out, ref = _both(m, 4096, 1000, 14 + m)
     assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("m,k,n", [(512, 8192, 512), (1000, 4096, 300)])
+def test_noalloc_k_split_plan(m, k, n):
+    # small-MN, large-K plans split every two-SM tile along K; the staging
+    # kernel zeroes C in the allocation-free variant too
+    assert B.gemm_i8_plan(m, k, n).split_k >= 2
+    out, ref = _both(m, k, n, 20 + m)
+    assert torch.equal(out, ref)
