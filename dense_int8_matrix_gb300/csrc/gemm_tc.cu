@@ -329,6 +329,31 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                                 tma_store_2d(&tmC, stg, static_cast<int32_t>(cs), ys);
                             bulk_commit();
                         }
+                    } else if constexpr (Cfg::TMA_STORE) {
+                        // C that TMA cannot store (unaligned rows or base): the
+                        // 32 x 32 block goes through the warp's staging buffer so
+                        // that every store (or atomic add) instruction covers 32
+                        // consecutive columns of one row
+                        const uint32_t stg = sEpi + e * kTcEpiStageBytes;
+                        uint32_t vals[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) vals[j] = GEMM_TC_OUT(j);
+                        __syncwarp();   // the previous block has been read out
+                        stage_rows32(stg, lane, vals);
+                        __syncwarp();
+                        const int64_t col = cs + lane;
+                        const int64_t ytop = static_cast<int64_t>(tm) * BM + q * 32;
+#pragma unroll 4
+                        for (int j = 0; j < 32; ++j) {
+                            const uint32_t v = staged_at(stg, j, lane);
+                            if (ytop + j < p.m && col < p.n) {
+                                uint32_t* o = static_cast<uint32_t*>(p.C) + (ytop + j) * p.ldc + col;
+                                if (add_into)
+                                    atomicAdd(o, v);
+                                else
+                                    *o = v;
+                            }
+                        }
                     } else {
                         if (row_valid && row < p.m) {
                             uint32_t* out = static_cast<uint32_t*>(p.C) + row * p.ldc + cs;

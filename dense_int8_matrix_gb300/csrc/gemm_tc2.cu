@@ -167,7 +167,9 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 // (`add`, the slices of a split tile): each lane holds the 32 values of its
 // row.  With C_TMA, the lanes fill the warp's 128B-swizzled 4 KiB staging
 // buffer and one TMA store (or reduce-add) moves the 32 x 32 box (clipped at
-// the edges of C); otherwise each lane stores (or atomically adds) its row.
+// the edges of C); otherwise, with 16-byte-aligned rows, each lane stores
+// its row, and with unaligned rows or adds the block is transposed through
+// the staging buffer into coalesced stores or atomics along the rows.
 template <bool C_TMA>
 __device__ __forceinline__ void store_slice32(const CUtensorMap* tmC, const T2Params& p, const uint32_t (&r)[32],
                                               uint32_t stg, int lane, int row, int ytop, int cs, bool c_vec,
@@ -188,19 +190,37 @@ __device__ __forceinline__ void store_slice32(const CUtensorMap* tmC, const T2Pa
                 tma_store_2d(tmC, stg, cs, ytop);
             bulk_commit();
         }
-    } else if (row < p.m) {
-        uint32_t* out = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc + cs;
-        if (add) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (cs + j < p.n) atomicAdd(out + j, r[j]);
-        } else if (c_vec && cs + 32 <= p.n) {
+    } else if (c_vec && !add) {
+        // 16-byte rows: each lane stores its row's 128 bytes
+        if (row < p.m && cs + 32 <= p.n) {
+            uint32_t* out = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc + cs;
 #pragma unroll
             for (int j = 0; j < 32; j += 4) *reinterpret_cast<uint4*>(out + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
-        } else {
+        } else if (row < p.m) {
+            uint32_t* out = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc + cs;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (cs + j < p.n) out[j] = r[j];
+        }
+    } else {
+        // unaligned rows, or adds: the 32 x 32 block goes through the warp's
+        // staging buffer so that every store (or atomic add) instruction
+        // covers 32 consecutive columns of one row
+        __syncwarp();   // the previous block has been read out
+        stage_rows32(stg, lane, r);
+        __syncwarp();
+        const int col = cs + lane;
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t v = staged_at(stg, j, lane);
+            const int rr = ytop + j;
+            if (rr < p.m && col < p.n) {
+                uint32_t* o = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(rr) * p.ldc + col;
+                if (add)
+                    atomicAdd(o, v);
+                else
+                    *o = v;
+            }
         }
     }
 }

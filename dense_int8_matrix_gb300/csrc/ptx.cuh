@@ -311,6 +311,26 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// One warp's 32 rows x 32 columns of 32-bit results, lane = row, written
+// into its 4 KiB staging buffer (128-byte rows, 16-byte chunks swizzled by
+// row & 7); then row j's 32 columns read back one per lane, so that stores
+// to global memory along a row of C are coalesced.
+__device__ __forceinline__ void stage_rows32(uint32_t stg, int lane, const uint32_t (&r)[32]) {
+    const uint32_t row_base = stg + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(row_base + ((c ^ (lane & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+}
+__device__ __forceinline__ uint32_t staged_at(uint32_t stg, int row, int col) {
+    return ld_shared_u32(stg + row * 128 + ((((col >> 2) ^ (row & 7))) << 4) + (col & 3) * 4);
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));

@@ -94,22 +94,32 @@ def test_workload_bf16_8192_sampled():
 TILES = [(bm, bn) for bm in (64, 128) for bn in (32, 64, 128, 256)] + [(256, 256)]
 
 
-def forced_plan(dtype, m, k, n, bm, bn, grid):
+def forced_plan(dtype, m, k, n, bm, bn, grid, split=1):
+    # the planner's plan with another tile and grid; split > 1 splits every
+    # tile into that many K slices, else the run decides (tail split only)
     p = B.gemm_plan_for_sms(dtype, m, k, n, torch.cuda.get_device_properties(0).multi_processor_count)
     p.bm, p.bn, p.grid = bm, bn, grid
+    if split > 1:
+        p.split_k, p.split_from = split, 0
+    else:
+        p.split_k, p.split_from = 1, max(1, p.tiles)
     return p
 
 
 @pytest.mark.parametrize("bm,bn", TILES)
-@pytest.mark.parametrize("grid", [4, 1000])
-def test_i8_every_tile(bm, bn, grid):
+@pytest.mark.parametrize("grid,split", [(4, 1), (1000, 1), (1000, 3)])
+def test_i8_every_tile(bm, bn, grid, split):
     # several tiles in both directions plus ragged tails; k = 2100 runs two
-    # full 1024-element accumulator chunks and a ragged third one
+    # full 1024-element accumulator chunks and a ragged third one (or, split
+    # 3 ways, slices of 11-11-11 K steps adding into C)
     m, k, n = 300, 2100, 700
     A = workloads.random_i8((m, k), 101)
     Bt = workloads.random_i8((n, k), 102)
-    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, bm, bn, grid)
-    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt, plan=p))
+    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, bm, bn, grid, split)
+    C1 = G.gpu_i8(A, Bt, plan=p)
+    G.assert_i8_exact(A, Bt, C1)
+    if split > 1:
+        assert torch.equal(C1, G.gpu_i8(A, Bt, plan=p))
 
 
 @pytest.mark.parametrize("bm,bn", TILES)
@@ -556,3 +566,26 @@ def test_i8_k_split_extremes_exact():
     Bt = torch.full((n, k), -128, dtype=torch.int8)
     C = G.gpu_i8(A, Bt, plan=p)
     assert torch.all(C == 16384 * k)
+
+
+@pytest.mark.parametrize("bm,bn", [(128, 128), (128, 256), (256, 256)])
+@pytest.mark.parametrize("grid", [6, 1000])
+def test_wide_tiles_unaligned_c(bm, bn, grid):
+    # n % 4 != 0: C cannot take TMA stores; the wide tiles transpose each
+    # 32 x 32 block through shared memory into stores / atomics along rows
+    # (grid 6: tail split, slices add; grid 1000: plain stores, then every
+    # tile split 2 ways)
+    m, k, n = 900, 2100, 701
+    A = workloads.random_i8((m, k), 71)
+    Bt = workloads.random_i8((n, k), 72)
+    if grid == 1000:
+        ps = forced_plan(B.GEMM_DTYPE_I8, m, k, n, bm, bn, grid, 2)
+        G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt, plan=ps))
+    p = forced_plan(B.GEMM_DTYPE_I8, m, k, n, bm, bn, grid)
+    C1 = G.gpu_i8(A, Bt, plan=p)
+    G.assert_i8_exact(A, Bt, C1)
+    assert torch.equal(C1, G.gpu_i8(A, Bt, plan=p))
+    Ab = workloads.random_bf16((m, 1000), 73)
+    Bb = workloads.random_bf16((n, 1000), 74)
+    pb = forced_plan(B.GEMM_DTYPE_BF16, m, 1000, n, bm, bn, grid)
+    G.assert_bf16_close(Ab, Bb, G.gpu_bf16(Ab, Bb, plan=pb))
