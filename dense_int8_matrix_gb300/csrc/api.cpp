@@ -155,22 +155,19 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     const bool sampled = trace_sample_call();
     if (p->path == GEMM_PATH_SKINNY) {
         if (skinny_tc_supported(p->m, p->n, p->k, A, Bt) && tensor_map_encoder_available()) {
-            // f16 copy of the small activation matrix; the same launch zeroes C,
-            // which the tensor-core kernel adds its partial sums into.  The
-            // skinny kernel starts while the staging kernel runs (programmatic
-            // dependent launch), so the two are timed as one unit.
+            // The prologue writes an f16 copy of the small activation matrix
+            // and zeroes C, which the tensor-core kernel adds its partial sums
+            // into.  Both are launched with programmatic stream serialization
+            // (each may start before the kernel in front of it ends), so the
+            // two are timed as one unit.
             void* ws = nullptr;
             const size_t a_bytes = static_cast<size_t>(p->m * p->k * 2);
             if (cudaMallocFromPoolAsync(&ws, a_bytes, ds->pool, stream) != cudaSuccess) return GEMM_ERR_CUDA;
             cudaError_t e;
             {
                 TraceScope t(GEMM_KERNEL_SKINNY, stream, sampled);
-                StageZero z;   // all of C
-                z.C = static_cast<int32_t*>(C);
-                z.m = p->m;
-                z.n = p->n;
-                e = launch_stage_i8(static_cast<const int8_t*>(A), nullptr, static_cast<uint16_t*>(ws), nullptr, p->m, 0,
-                                    p->k, p->k, z, ds->err_word, ds->num_sms, stream);
+                e = launch_skinny_prologue(static_cast<const int8_t*>(A), static_cast<uint16_t*>(ws),
+                                           static_cast<int32_t*>(C), p->m, p->n, p->k, ds->num_sms, stream);
                 if (e == cudaSuccess) {
                     trace_count(GEMM_KERNEL_STAGE);
                     e = launch_skinny_tc(static_cast<const int8_t*>(Bt), static_cast<const uint16_t*>(ws),

@@ -36,6 +36,17 @@
 // Work split ("stream-K"): the (128-row tile, stage) iterations are numbered
 // tile-major and every CTA takes an equal contiguous range, so all SMs
 // stream the same number of Bt bytes.
+//
+// Back-to-back calls overlap (programmatic dependent launch): every CTA lets
+// the next kernel in the stream launch as soon as it starts, so the next
+// call's prologue (A to f16, C zeroed: one small CTA per SM beside this one)
+// is resident, waiting, and the next skinny kernel is launched, before this
+// one ends.  Each of its CTAs takes an SM the moment this kernel's CTA there
+// exits and at once asks L2 for its first L2_AHEAD stages of Bt (a prefetch
+// changes no data, so it needs no wait); it loads them into shared memory,
+// reads its activations and adds into C only after the grid dependency wait.
+// HBM keeps streaming through the gap between two calls: this kernel's drain,
+// the launch of the next, and the prologue's dependent wait.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -79,16 +90,28 @@ struct SkCfg {
     static constexpr int ACT_STAGES = NP >= 64 ? 2 : 4;
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = NP / 2;                    // columns per epilogue warp
+    // Bt stages asked of L2 ahead of the loads into shared memory (32 KiB
+    // each; 152 CTAs x 12 stages = 57 MiB at most, within the 129 MiB L2).
+    // Measured on GB300 in back-to-back calls (k = n = 8192): 18.3 against
+    // 18.9 us per call at m = 1; at m = 64 the prefetch cost more than it
+    // saved (22.4 against 21.6 us), so NP >= 64 does without.
+    static constexpr int L2_AHEAD = NP >= 64 ? 0 : 12;
+    // barriers (8 B each), the TMEM address and the abort flag
+    static constexpr int CTRL = 8 * (3 * BT_STAGES + 2 * ACT_STAGES + 2 * ABUF_BARS + 5) + 8;
+    // + up to 1023 B to align the ring to the 1024 B the 128-byte swizzle needs
     static constexpr size_t SMEM =
-        static_cast<size_t>(BT_STAGES) * kSkBtStage + static_cast<size_t>(ACT_STAGES) * ACT_STAGE + 1024 + 1024;
+        static_cast<size_t>(BT_STAGES) * kSkBtStage + static_cast<size_t>(ACT_STAGES) * ACT_STAGE + 512 + 1024;
     static_assert(ABUFS * 128 + 2 * NP <= TMEM_COLS, "TMEM budget");
-    static_assert(SMEM <= 232448, "shared memory");
+    static_assert(CTRL <= 512, "control block");
+    // with the 1 KiB the SM reserves per CTA, one skinny CTA and one prologue
+    // CTA fit in the SM's 228 KiB of shared memory
+    static_assert(SMEM + 1024 + 1024 <= 233472, "shared memory");
 };
 
 struct SkParams {
     int32_t* C;
     int* err;
-    int m, n;
+    int m, n, k;
     int num_sb;       // stages of 256 K per tile
     int tiles;        // ceil(n / 128)
     int64_t iters;    // tiles * num_sb
@@ -166,6 +189,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // the next kernel in the stream (the next call's prologue) may launch
+    pdl_launch_dependents();
 
     if (warp == 0 && lane == 0) {
         // the descriptors are fetched while the CTA sets up
@@ -206,6 +231,20 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // ------------------------------------------------------- TMA: Bt --
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
+            // L2 prefetch, L2_AHEAD stages ahead of the loads: the first
+            // ones before the grid dependency wait (the kernel before may
+            // still be running; a prefetch reads nothing into this CTA)
+            Cursor pc = cursor_at(p, lo);
+            int64_t pi = lo;
+            auto prefetch_next = [&]() {
+                const int x = pc.sb * 256;
+                tma_prefetch_l2_2d(&tmB, x, pc.tile * 128);
+                if (x + 128 < p.k) tma_prefetch_l2_2d(&tmB, x + 128, pc.tile * 128);
+                ++pi;
+                pc.advance(p.num_sb);
+            };
+            while (pi < hi && pi < lo + Cfg::L2_AHEAD) prefetch_next();
+            pdl_wait();
             uint32_t n_iss = 0;
             Cursor c = cursor_at(p, lo);
             for (int64_t i = lo; i < hi; ++i, ++n_iss, c.advance(p.num_sb)) {
@@ -218,6 +257,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 mbar_arrive_expect_tx(fb, kSkBtStage);
                 tma_load_2d(dst, &tmB, x, tile * 128, fb, pol);
                 tma_load_2d(dst + kSkBtBox, &tmB, x + 128, tile * 128, fb, pol);
+                if (Cfg::L2_AHEAD > 0 && pi < hi) prefetch_next();
             }
             // the last BT_STAGES copies may still be in flight (earlier ones
             // landed before their slot was reused)
@@ -227,7 +267,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     } else if (warp == 2) {
         // ---------------------------------------------- TMA: activations --
         if (lane == 0) {
-            pdl_wait();   // the activations are written by the staging kernel just before
+            pdl_wait();   // the activations are written by the prologue just before
             const uint64_t pol = policy_evict_last();
             uint32_t n_iss = 0;
             Cursor c = cursor_at(p, lo);
@@ -386,7 +426,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             mbar_arrive(acce0);
             mbar_arrive(acce0 + 8u);
         }
-        pdl_wait();   // C is zeroed by the staging kernel just before
+        pdl_wait();   // C is zeroed by the prologue just before
         uint32_t ch = 0;
         Cursor c = cursor_at(p, lo);
         for (int64_t i = lo; i < hi; ++i, c.advance(p.num_sb)) {
@@ -466,6 +506,7 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     p.err = err;
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
     p.num_sb = static_cast<int>((k + 255) / 256);
     p.tiles = static_cast<int>((n + 127) / 128);
     p.iters = static_cast<int64_t>(p.tiles) * p.num_sb;
@@ -475,10 +516,10 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     auto kern = skinny_tc_kernel<NP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM));
     if (e != cudaSuccess) return e;
-    // Programmatic dependent launch: the kernel may start while the staging
-    // kernel before it runs.  Bt is not written by that kernel (which itself
-    // started after all earlier work in the stream), so its stream starts at
-    // once; the activation loads and the writes of C wait for it.
+    // Programmatic dependent launch: the kernel may start while the prologue
+    // before it (and, through it, the previous call's kernel) still runs.
+    // Until its grid dependency wait it only sets up and prefetches Bt into
+    // L2; every load into shared memory and every write of C comes after.
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cudaLaunchAttribute attr[1];

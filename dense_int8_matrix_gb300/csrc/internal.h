@@ -191,6 +191,14 @@ cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah
 // ---- skinny path on the tensor cores (gemm_skinny_tc.cu) --------------------
 // Needs k % 16 == 0 (TMA row pitch of int8 Bt) and 16-byte aligned A and Bt.
 bool skinny_tc_supported(int64_t m, int64_t n, int64_t k, const void* A, const void* Bt);
+// Its prologue (stage.cu): A (m x k int8, k % 16 == 0, A and A16 16-byte
+// aligned) to f16 in A16 and all of C (m x n) zeroed, by one small CTA per SM
+// that fits beside a running skinny CTA.  Launched with programmatic stream
+// serialization, it becomes resident while the kernel before it still runs
+// (and lets the skinny kernel after it launch), and touches memory only once
+// that kernel has completed.
+cudaError_t launch_skinny_prologue(const int8_t* A, uint16_t* A16, int32_t* C, int64_t m, int64_t n, int64_t k,
+                                   int num_sms, cudaStream_t stream);
 // A16: the m x k activations as f16 (row pitch k); C must be zero (the kernel
 // adds its partial sums into it).
 cudaError_t launch_skinny_tc(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* err, int64_t m, int64_t n,

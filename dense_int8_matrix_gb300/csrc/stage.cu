@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -283,6 +284,35 @@ __global__ void __launch_bounds__(256) stage_b16_rows_kernel(const uint16_t* __r
     }
 }
 
+// Skinny-path prologue: A to f16 and all of C zeroed.  128 threads at <= 32
+// registers (4,096 registers) and no shared memory fit on an SM beside a
+// running skinny tensor-core CTA (640 threads x 96 registers, <= 226 KiB of
+// shared memory), so with programmatic stream serialization every CTA of this
+// kernel is resident, and has let the skinny kernel behind it launch, while
+// the kernel before it still runs; the skinny CTAs then take each SM as soon
+// as it is free and stream their Bt into L2 while this kernel waits.  Nothing
+// is read or written before the wait: A, A16 and C may all be in use by the
+// kernel before.
+constexpr int kProThreads = 128;
+__global__ void __launch_bounds__(kProThreads, 16) skinny_prologue_kernel(const uint4* __restrict__ A,
+                                                                          uint4* __restrict__ A16, int64_t itemsA,
+                                                                          const StageZero z) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t i0 = t; i0 < itemsA; i0 += 2 * stride) {
+        uint4 v[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (i0 + u * stride < itemsA) v[u] = ld_stream(A + i0 + u * stride);
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (i0 + u * stride < itemsA) convert16(v[u], A16 + 2 * (i0 + u * stride));
+    }
+    zero_work(z, t, stride);
+}
+
 int grid_for(int64_t items, int num_sms) {
     // 8 resident 256-thread blocks per SM, grid a multiple of the SM count
     int64_t want = (items + 255) / 256;
@@ -322,6 +352,29 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
         stage_i8_rows_kernel<<<grid_for(items > zi ? items : zi, num_sms), 256, 0, stream>>>(
             A, Bt, reinterpret_cast<uint4*>(Ah), reinterpret_cast<uint4*>(Bh), m, n, k, k_pitch, z);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_skinny_prologue(const int8_t* A, uint16_t* A16, int32_t* C, int64_t m, int64_t n, int64_t k,
+                                   int num_sms, cudaStream_t stream) {
+    StageZero z;   // all of C
+    z.C = C;
+    z.m = m;
+    z.n = n;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms), 1, 1);
+    cfg.blockDim = dim3(kProThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_prologue_kernel, reinterpret_cast<const uint4*>(A),
+                                       reinterpret_cast<uint4*>(A16), m * k / 16, z);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
