@@ -444,6 +444,80 @@ def test_i8_skinny_two_streams():
     assert B.gemm_device_error() == (B.GEMM_OK, 0)
 
 
+def test_i8_skinny_chain_output_feeds_next_weights():
+    # Back-to-back skinny calls on one stream overlap: each call's kernels
+    # start while the previous call's still run (programmatic dependent
+    # launch).  Here every call's Bt is the bytes of the previous call's C,
+    # so a kernel that read its Bt before the previous call had finished
+    # would multiply stale bytes.  Each C is 16 x 8192 int32 = 512 KiB,
+    # read as the next call's Bt of 512 x 1024 int8.
+    m, k, n = 16, 8192, 8192
+    m2, k2, n2 = 8, 1024, 512
+    A1 = workloads.random_i8((m, k), 301)
+    Bt1 = workloads.random_i8((n, k), 302)
+    A2 = [workloads.random_i8((m2, k2), 303 + i) for i in range(3)]
+    # the chain on the CPU: C1 = A1 Bt1; then three calls whose Bt is the
+    # previous C's bytes (every one of them 512 KiB)
+    C1 = oracle.gemm_i8(A1.numpy(), Bt1.numpy())
+    want = [C1]
+    prev = C1
+    for i in range(3):
+        bt = np.ascontiguousarray(prev).view(np.int8).reshape(n2, k2)
+        out = oracle.gemm_i8(A2[i].numpy(), bt)
+        # later links multiply a 8 x 512 C, so it is embedded in a 512 KiB
+        # buffer of the previous C's remaining bytes: the GPU side does the same
+        # by writing into the first rows of the buffer it reads next
+        nxt = np.ascontiguousarray(prev).copy().view(np.int32).reshape(-1)
+        nxt[:out.size] = out.reshape(-1)
+        prev = nxt.reshape(m, n)
+        want.append(out)
+    bufs = [torch.full((m, n), -7, dtype=torch.int32, device="cuda") for _ in range(4)]
+    dA1, dB1 = A1.cuda(), Bt1.cuda()
+    dA2 = [a.cuda() for a in A2]
+    p1 = B.gemm_i8_plan(m, k, n)
+    p2 = B.gemm_i8_plan(m2, k2, n2)
+    torch.cuda.synchronize()
+    B.gemm_i8_run(p1, dA1, dB1, bufs[0])
+    for i in range(3):
+        # the next buffer starts as a copy of the one being read (torch's copy
+        # kernel sits between the two calls), then its first rows take C
+        bufs[i + 1].copy_(bufs[i])
+        out = bufs[i + 1].view(-1)[: m2 * n2].view(m2, n2)
+        B.gemm_i8_run(p2, dA2[i], bufs[i].view(torch.int8).view(n2, k2), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bufs[0].cpu().numpy(), want[0])
+    for i in range(3):
+        got = bufs[i + 1].view(-1)[: m2 * n2].view(m2, n2).cpu().numpy()
+        assert np.array_equal(got, want[i + 1]), "link %d differs" % (i + 1)
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
+def test_i8_skinny_chain_direct_alias():
+    # Two skinny calls back to back with nothing between them: the second
+    # call's Bt is the first call's C.  Only the grid-dependency wait orders
+    # the second call's reads of Bt after the first call's writes of C.
+    m, k, n = 16, 8192, 8192
+    m2, k2, n2 = 8, 1024, 512
+    A1 = workloads.random_i8((m, k), 311)
+    Bt1 = workloads.random_i8((n, k), 312)
+    A2 = workloads.random_i8((m2, k2), 313)
+    C1 = oracle.gemm_i8(A1.numpy(), Bt1.numpy())
+    want2 = oracle.gemm_i8(A2.numpy(), np.ascontiguousarray(C1).view(np.int8).reshape(n2, k2))
+    dA1, dB1, dA2 = A1.cuda(), Bt1.cuda(), A2.cuda()
+    p1 = B.gemm_i8_plan(m, k, n)
+    p2 = B.gemm_i8_plan(m2, k2, n2)
+    for rep in range(20):
+        C = torch.full((m, n), -7, dtype=torch.int32, device="cuda")
+        C2 = torch.full((m2, n2), -7, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        B.gemm_i8_run(p1, dA1, dB1, C)
+        B.gemm_i8_run(p2, dA2, C.view(torch.int8).view(n2, k2), C2)
+        torch.cuda.synchronize()
+        assert np.array_equal(C.cpu().numpy(), C1)
+        assert np.array_equal(C2.cpu().numpy(), want2), "repetition %d" % rep
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
 @pytest.mark.parametrize("m", [64, 128])
 def test_i8_skinny_extremes(m):
     k, n = 16384, 1000
