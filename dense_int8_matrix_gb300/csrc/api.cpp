@@ -80,6 +80,13 @@ struct TraceRec {
     cudaEvent_t start, stop;
 };
 
+std::mutex g_attr_mu;
+struct AttrDone {
+    const void* kern;
+    int dev;
+};
+std::vector<AttrDone> g_attr_done;
+
 std::mutex g_trace_mu;
 bool g_trace_on = false;
 int32_t g_trace_every = 1;
@@ -514,6 +521,21 @@ gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const voi
 }
 
 }  // namespace
+
+cudaError_t gemm::kernel_attrs_once(const void* kern, int smem_bytes, bool max_carveout) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    for (const AttrDone& d : g_attr_done)
+        if (d.kern == kern && d.dev == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e == cudaSuccess && max_carveout)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e == cudaSuccess) g_attr_done.push_back(AttrDone{kern, dev});
+    return e;
+}
 
 extern "C" {
 

@@ -514,7 +514,7 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     if (grid > p.iters) grid = p.iters;
     p.iters32 = (p.iters * (grid + 1)) < (int64_t(1) << 32) ? 1 : 0;
     auto kern = skinny_tc_kernel<NP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM));
+    cudaError_t e = kernel_attrs_once(reinterpret_cast<const void*>(kern), static_cast<int>(Cfg::SMEM), false);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel may start while the prologue
     // before it (and, through it, the previous call's kernel) still runs.

@@ -433,10 +433,7 @@ bool encode_operand_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t
 // Opt in to the kernel's dynamic shared memory and ask for the largest
 // shared-memory carveout, so that the CTAs per SM the planner counts on fit.
 cudaError_t configure_kernel(const void* kern, size_t smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    return kernel_attrs_once(kern, static_cast<int>(smem), true);
 }
 
 // Tensor map of C (m x n, 4-byte elements, row pitch ldc elements) for TMA

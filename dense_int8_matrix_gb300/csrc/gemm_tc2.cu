@@ -456,12 +456,7 @@ const void* tc2_kernel_ptr() {
     return reinterpret_cast<const void*>(gemm_tc2_kernel<INT_OUT, C_TMA>);
 }
 
-cudaError_t configure2(const void* kern) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kT2Smem));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
-}
+cudaError_t configure2(const void* kern) { return kernel_attrs_once(kern, static_cast<int>(kT2Smem), true); }
 
 }  // namespace
 

@@ -217,4 +217,11 @@ cudaError_t launch_selftest_wait(int* err, uint64_t timeout_ns, cudaStream_t str
 bool tensor_map_encoder_available();
 void* tensor_map_encoder();   // cuTensorMapEncodeTiled, or nullptr
 
+// ---- kernel attributes (api.cpp) ---------------------------------------------
+// Opts `kern` in to `smem_bytes` of dynamic shared memory (and, if asked, the
+// largest shared-memory carveout) on the current device, once per device and
+// kernel for the life of the process: cudaFuncSetAttribute costs host time on
+// every call, which on short launches is more than the GPU time.
+cudaError_t kernel_attrs_once(const void* kern, int smem_bytes, bool max_carveout);
+
 }  // namespace gemm

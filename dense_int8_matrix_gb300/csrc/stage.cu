@@ -331,8 +331,8 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
                            reinterpret_cast<uintptr_t>(Ah) | reinterpret_cast<uintptr_t>(Bh)) &
                           15u) == 0;
     if (k == k_pitch && (k % 16) == 0 && aligned && (m + n) * k >= kBulkMinBytes && err != nullptr) {
-        cudaError_t e = cudaFuncSetAttribute(stage_i8_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kBulkSmem));
+        cudaError_t e = kernel_attrs_once(reinterpret_cast<const void*>(stage_i8_bulk_kernel),
+                                          static_cast<int>(kBulkSmem), false);
         if (e != cudaSuccess) return e;
         const int64_t chunks = ((m * k + kBulkChunk - 1) / kBulkChunk) + ((n * k + kBulkChunk - 1) / kBulkChunk);
         const int grid = static_cast<int>(chunks < num_sms ? chunks : num_sms);

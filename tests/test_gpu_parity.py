@@ -518,6 +518,20 @@ def test_i8_skinny_chain_direct_alias():
     assert B.gemm_device_error() == (B.GEMM_OK, 0)
 
 
+@pytest.mark.parametrize("m,k,n", [(16, 4096, 1024), (100, 2048, 640)])
+def test_i8_skinny_c_offset(m, k, n):
+    # C starting 4 bytes into an allocation (C needs only 4-byte alignment):
+    # every element written exactly, nothing outside C touched
+    A = workloads.random_i8((m, k), 321 + m)
+    Bt = workloads.random_i8((n, k), 322 + m)
+    base = torch.full((m * n + 4,), -7, dtype=torch.int32, device="cuda")
+    C = base[1:1 + m * n].view(m, n)
+    B.gemm_i8_run(B.gemm_i8_plan(m, k, n), A.cuda(), Bt.cuda(), C)
+    torch.cuda.synchronize()
+    G.assert_i8_exact(A, Bt, C.cpu())
+    assert base[0].item() == -7 and torch.all(base[1 + m * n:] == -7)
+
+
 @pytest.mark.parametrize("m", [64, 128])
 def test_i8_skinny_extremes(m):
     k, n = 16384, 1000
