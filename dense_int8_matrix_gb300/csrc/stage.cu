@@ -12,10 +12,14 @@
 // in f16) leaves x.  Memory-bound: 1 byte read and 2 written per element.
 //
 // Large contiguous operands go through shared memory with bulk copies
-// (cp.async.bulk): 16 KiB int8 chunks in, widened in shared memory, 32 KiB f16
-// chunks out.  Measured on GB300 for the 4096^3 operands (32 MiB in, 64 MiB
-// out): 20.5 us, against 24.8 us for per-thread 16-byte loads and stores;
-// reading 32 MiB alone takes 8.2 us and writing 64 MiB alone 12.3 us.
+// (cp.async.bulk): 8 KiB int8 chunks in (four in flight), widened in shared
+// memory, 16 KiB f16 chunks out, three 66 KiB CTAs per SM.  Measured on GB300
+// for the 4096^3 operands (32 MiB in, 64 MiB out) inside the GEMM step: 20.4
+// us per launch, against 24.8 us with one CTA per SM (16 KiB chunks, four or
+// up to ten in flight: 23.1-24.8 us) -- a CTA converts a chunk between two
+// barriers, so more CTAs, not more loads in flight, keep HBM busy; 4 KiB
+// chunks at six CTAs per SM measured the same (19.9 us).  Per-thread 16-byte
+// loads and stores took 24.8 us.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -92,11 +96,13 @@ __device__ __forceinline__ void zero_work(const StageZero& z, int64_t i0, int64_
 }
 
 // ---- bulk-copy staging -------------------------------------------------
-constexpr int kBulkChunk = 16384;                  // int8 bytes per chunk
+constexpr int kBulkChunk = 8192;                   // int8 bytes per chunk
 constexpr int kBulkDepth = 4;                      // chunks in flight per CTA
 constexpr int kBulkThreads = 256;
 constexpr size_t kBulkSmem = static_cast<size_t>(kBulkDepth) * kBulkChunk + 2 * 2 * kBulkChunk + 1024;
 constexpr int64_t kBulkMinBytes = int64_t(8) << 20;   // smaller problems: per-thread kernel
+constexpr int kBulkCtasPerSm = 3;
+static_assert(kBulkCtasPerSm * (kBulkSmem + 1024) <= 233472, "bulk staging CTAs per SM");
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -138,8 +144,8 @@ __global__ void __launch_bounds__(kBulkThreads) stage_i8_bulk_kernel(const uint8
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sin = base;                                 // kBulkDepth x 16 KiB
-    const uint32_t sout = base + kBulkDepth * kBulkChunk;      // 2 x 32 KiB
+    const uint32_t sin = base;                                 // kBulkDepth x 8 KiB
+    const uint32_t sout = base + kBulkDepth * kBulkChunk;      // 2 x 16 KiB
     uint8_t* const gin = smem_raw + (base - smem_u32(smem_raw));
     uint8_t* const gout = gin + kBulkDepth * kBulkChunk;
     __shared__ __align__(8) uint64_t full[kBulkDepth];
@@ -335,7 +341,9 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
                                           static_cast<int>(kBulkSmem), false);
         if (e != cudaSuccess) return e;
         const int64_t chunks = ((m * k + kBulkChunk - 1) / kBulkChunk) + ((n * k + kBulkChunk - 1) / kBulkChunk);
-        const int grid = static_cast<int>(chunks < num_sms ? chunks : num_sms);
+        // three CTAs per SM (66 KiB of shared memory each)
+        const int64_t cap = static_cast<int64_t>(kBulkCtasPerSm) * num_sms;
+        const int grid = static_cast<int>(chunks < cap ? chunks : cap);
         stage_i8_bulk_kernel<<<grid, kBulkThreads, kBulkSmem, stream>>>(
             reinterpret_cast<const uint8_t*>(A), reinterpret_cast<const uint8_t*>(Bt), reinterpret_cast<uint8_t*>(Ah),
             reinterpret_cast<uint8_t*>(Bh), m * k, n * k, z, err);
