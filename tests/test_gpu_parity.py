@@ -444,6 +444,26 @@ def test_i8_skinny_two_streams():
     assert B.gemm_device_error() == (B.GEMM_OK, 0)
 
 
+@pytest.mark.parametrize("m,k,n", [
+    (7, 4096, 4096),      # 32 tiles of 128 rows of Bt
+    (32, 1024, 16384),    # 128 tiles, 4 stages each
+    (3, 2048, 1900),      # 15 tiles, the last one ragged
+    (31, 1296, 2560),     # ragged last stage (16 K)
+    (17, 8192, 8192),     # m just above a 16-row MMA
+])
+def test_i8_skinny_more_shapes(m, k, n):
+    # stream-K ranges that start and end mid-tile and mid-chunk on tiles of
+    # every fill, then the extremes: every 1024-K chunk reaches 2^24
+    A = workloads.random_i8((m, k), 331 + m)
+    Bt = workloads.random_i8((n, k), 332 + m)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt))
+    A = torch.full((m, k), -128, dtype=torch.int8)
+    Bt = torch.full((n, k), -128, dtype=torch.int8)
+    Bt[1::3] = 127
+    C = G.gpu_i8(A, Bt)
+    assert torch.all(C[:, 0::3] == 16384 * k) and torch.all(C[:, 1::3] == -128 * 127 * k)
+
+
 def test_i8_skinny_chain_output_feeds_next_weights():
     # Back-to-back skinny calls on one stream overlap: each call's kernels
     # start while the previous call's still run (programmatic dependent
