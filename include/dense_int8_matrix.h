@@ -26,7 +26,12 @@
  * Asynchrony: gemm_*_run only enqueues work on `stream` (a cudaStream_t;
  * NULL = the legacy default stream) and returns.  Launch errors are returned
  * as GEMM_ERR_CUDA.  Errors found while kernels run (a wait that ran past its
- * time limit) are reported by gemm_device_error().
+ * time limit) are reported by gemm_device_error().  The library's kernels
+ * are launched with programmatic stream serialization, so a call's kernels
+ * may start (set up, prefetch into L2) before the work in front of them on
+ * the stream has finished; none of them reads or writes A, Bt, C or scratch
+ * before that work has completed, so stream order holds as usual.  C must
+ * not overlap A or Bt of the same call.
  *
  * Thread safety: every entry point may be called from several host threads.
  */
@@ -220,11 +225,14 @@ GEMM_API gemm_status gemm_device_error(void *stream, int32_t *code);
  * the (every+1)-th, ...) records a pair of CUDA events on its stream around
  * each timed unit (at most `capacity` units are recorded): the staging
  * launch and the GEMM launch of the tensor path separately (kinds STAGE and
- * TC); on the skinny tensor-core path the staging launch and the skinny
- * launch together, as kind SKINNY, because the skinny kernel starts while
- * the staging kernel runs (programmatic dependent launch).  Calls that are
- * not sampled record no events, so sampling keeps the timing from slowing
- * the work it measures.  gemm_trace_collect waits for the events and writes,
+ * TC); on the skinny tensor-core path the prologue launch (A to f16, C
+ * zeroed) and the skinny launch together, as kind SKINNY, because the skinny
+ * kernel starts while the prologue runs (programmatic dependent launch).
+ * Calls that are not sampled record no events, so sampling keeps the timing
+ * from slowing the work it measures.  Back-to-back skinny calls on one
+ * stream overlap (each call's kernels start before the previous call's
+ * end); an event recorded between two calls, as a sampled call records,
+ * makes them run one after the other.  gemm_trace_collect waits for the events and writes,
  * per kind (arrays of GEMM_KERNEL_KINDS entries): the summed device time in
  * ms of the timed units, the number of timed units, and the number of
  * launches counted; it then disables tracing.  every >= 1.
