@@ -75,6 +75,25 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device: str) -> float:
+    """The slowest rank's time: every rank runs an independent replica, so
+    the job takes as long as its slowest one.  All ranks must call it."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def whole_job_value(world: int, ops_per_step: float, ms_per_step: float) -> float:
+    """Tera-operations per second of all ranks together (weak scaling: each
+    rank does one step's work per step)."""
+    return world * ops_per_step / (ms_per_step / 1000.0) / 1e12
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -339,17 +358,11 @@ def run_ours(args):
     st, code = B.gemm_device_error()
     if st != B.GEMM_OK:
         raise RuntimeError("device error during bench: code %d" % code)
-    max_ms = elapsed_ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
-        dist.barrier()
+    max_ms = max_over_ranks(elapsed_ms, world, "cuda")
 
     ops = 2.0 * m * n * k
     ms_per_step = max_ms / args.steps
-    value = world * ops / (ms_per_step / 1000.0) / 1e12
+    value = whole_job_value(world, ops, ms_per_step)
 
     # end to end through the host-buffer entry point: H2D of A and Bt,
     # the GEMM, D2H of C, inside the timed region
