@@ -14,10 +14,9 @@
 //
 // Roles, per CTA (20 warps):
 //   warp 0      TMA: the int8 Bt boxes (128 rows x 256 B, 128-byte swizzle)
-//               into a 5-6-deep ring (it must cover the loaded HBM latency,
-//               ~2 us on GB300);
+//               into a 3-deep ring;
 //   warp 2      TMA: the f16 activation boxes (NP rows x 256 K) into a
-//               2-4-deep ring (they are re-read by every CTA and stay in L2);
+//               2-6-deep ring (they are re-read by every CTA and stay in L2);
 //   warps 4-11  two groups of four warps that take the stages in turn (one
 //               warp of a group per TMEM lane quarter): each lane reads its
 //               Bt row (256 int8) from shared memory, releases the stage,
@@ -42,11 +41,17 @@
 // call's prologue (A to f16, C zeroed: one small CTA per SM beside this one)
 // is resident, waiting, and the next skinny kernel is launched, before this
 // one ends.  Each of its CTAs takes an SM the moment this kernel's CTA there
-// exits and at once asks L2 for its first L2_AHEAD stages of Bt (a prefetch
-// changes no data, so it needs no wait); it loads them into shared memory,
-// reads its activations and adds into C only after the grid dependency wait.
-// HBM keeps streaming through the gap between two calls: this kernel's drain,
-// the launch of the next, and the prologue's dependent wait.
+// exits and sets up; it loads Bt and its activations and adds into C only
+// after the grid dependency wait.
+//
+// Ring depths, measured on GB300 in back-to-back calls (k = n = 8192): a
+// shallow Bt ring is faster.  A call is bound by the latency of its first
+// stages, not by the stream (which runs at DRAM rate either way), and a deep
+// ring makes every CTA queue its whole ring at once: m = 1 with 6 / 4 / 3 / 2
+// stages 17.7 / 17.3 / 16.5 / 18.5 us per call, m = 64 with 5 / 3 stages
+// (activation slots 2 / 4) 21.6 / 20.2 us.  Prefetching the first Bt stages
+// into L2 before the wait cost time on top (m = 1, 3 stages: 17.1 us with 4
+// stages ahead, 17.0 with 12, 16.5 with none).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -82,20 +87,13 @@ struct SkCfg {
     // TMEM: ABUFS operand buffers of 128 columns and two NP-column accumulators.
     static constexpr int ABUFS = NP >= 128 ? 2 : 3;
     static constexpr int ABUF_BARS = 2 * ABUFS;
-    // The activation ring must cover the MMA-to-refill latency (an L2 round
-    // trip after the MMA two or more stages back completes); the Bt ring the
-    // HBM latency.  NP = 128 activation stages are 64 KB: the Bt ring gets
-    // what is left.
-    static constexpr int BT_STAGES = NP >= 128 ? 3 : (NP >= 32 ? 5 : 6);
-    static constexpr int ACT_STAGES = NP >= 64 ? 2 : 4;
+    // Three Bt stages (see the measurements above); the activation ring gets
+    // the room left, an even number of slots so that each slot always serves
+    // the same MMA issuer (NP = 128 activation stages are 64 KB).
+    static constexpr int BT_STAGES = 3;
+    static constexpr int ACT_STAGES = NP >= 128 ? 2 : (NP == 32 ? 6 : 4);
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = NP / 2;                    // columns per epilogue warp
-    // Bt stages asked of L2 ahead of the loads into shared memory (32 KiB
-    // each; 152 CTAs x 12 stages = 57 MiB at most, within the 129 MiB L2).
-    // Measured on GB300 in back-to-back calls (k = n = 8192): 18.3 against
-    // 18.9 us per call at m = 1; at m = 64 the prefetch cost more than it
-    // saved (22.4 against 21.6 us), so NP >= 64 does without.
-    static constexpr int L2_AHEAD = NP >= 64 ? 0 : 12;
     // barriers (8 B each), the TMEM address and the abort flag
     static constexpr int CTRL = 8 * (3 * BT_STAGES + 2 * ACT_STAGES + 2 * ABUF_BARS + 5) + 8;
     // + up to 1023 B to align the ring to the 1024 B the 128-byte swizzle needs
@@ -111,7 +109,7 @@ struct SkCfg {
 struct SkParams {
     int32_t* C;
     int* err;
-    int m, n, k;
+    int m, n;
     int num_sb;       // stages of 256 K per tile
     int tiles;        // ceil(n / 128)
     int64_t iters;    // tiles * num_sb
@@ -231,20 +229,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // ------------------------------------------------------- TMA: Bt --
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            // L2 prefetch, L2_AHEAD stages ahead of the loads: the first
-            // ones before the grid dependency wait (the kernel before may
-            // still be running; a prefetch reads nothing into this CTA)
-            Cursor pc = cursor_at(p, lo);
-            int64_t pi = lo;
-            auto prefetch_next = [&]() {
-                const int x = pc.sb * 256;
-                tma_prefetch_l2_2d(&tmB, x, pc.tile * 128);
-                if (x + 128 < p.k) tma_prefetch_l2_2d(&tmB, x + 128, pc.tile * 128);
-                ++pi;
-                pc.advance(p.num_sb);
-            };
-            while (pi < hi && pi < lo + Cfg::L2_AHEAD) prefetch_next();
-            pdl_wait();
+            pdl_wait();   // the kernel before may still be running (and writing Bt)
             uint32_t n_iss = 0;
             Cursor c = cursor_at(p, lo);
             for (int64_t i = lo; i < hi; ++i, ++n_iss, c.advance(p.num_sb)) {
@@ -257,7 +242,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 mbar_arrive_expect_tx(fb, kSkBtStage);
                 tma_load_2d(dst, &tmB, x, tile * 128, fb, pol);
                 tma_load_2d(dst + kSkBtBox, &tmB, x + 128, tile * 128, fb, pol);
-                if (Cfg::L2_AHEAD > 0 && pi < hi) prefetch_next();
             }
             // the last BT_STAGES copies may still be in flight (earlier ones
             // landed before their slot was reused)
@@ -506,7 +490,6 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     p.err = err;
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
-    p.k = static_cast<int>(k);
     p.num_sb = static_cast<int>((k + 255) / 256);
     p.tiles = static_cast<int>((n + 127) / 128);
     p.iters = static_cast<int64_t>(p.tiles) * p.num_sb;
@@ -518,8 +501,8 @@ cudaError_t launch_np(const int8_t* Bt, const uint16_t* A16, int32_t* C, int* er
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel may start while the prologue
     // before it (and, through it, the previous call's kernel) still runs.
-    // Until its grid dependency wait it only sets up and prefetches Bt into
-    // L2; every load into shared memory and every write of C comes after.
+    // Until its grid dependency wait it only sets up; every load and every
+    // write of C comes after.
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cudaLaunchAttribute attr[1];

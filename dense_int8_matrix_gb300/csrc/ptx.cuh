@@ -117,17 +117,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* desc, int3
         : "memory");
 }
 
-// 2-D tiled prefetch of one box into L2 (no shared memory, no barrier).  A
-// prefetch changes no data: L2 is the point of coherence of every load and
-// atomic of this GPU, so it may be issued at any time, even before a grid
-// dependency wait.  The caller keeps x inside the tensor.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(desc)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // 2-D tiled store of one box from shared memory (bulk-group completion).
 // Elements of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int32_t x, int32_t y) {
