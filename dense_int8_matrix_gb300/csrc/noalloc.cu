@@ -17,8 +17,9 @@
 // come before any stream capture.
 //
 // All calls share the one array and it keeps the last call's contents.  The
-// staging kernel overwrites every element the GEMM reads (the pad columns of
-// each row are never read), and the variant's time-out word is cleared at the
+// staging kernel (or, on the skinny path, the prologue that writes the f16
+// copy of A) overwrites every element the GEMM reads (the pad columns of each
+// row are never read), and the variant's time-out word is cleared at the
 // start of each call.  Calls whose work overlaps on the GPU (on different
 // streams, or on different host threads without ordering) race on the array
 // and give wrong results: order them.
@@ -102,7 +103,7 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
         return GEMM_ERR_MISALIGNED;
     const bool skinny = p->path == GEMM_PATH_SKINNY;
     if (skinny) {
-        if (p->m > 128) return GEMM_ERR_INVALID_ARG;
+        if (p->m > 128 || p->k > GEMM_I8_MAX_K) return GEMM_ERR_INVALID_ARG;
     } else {
         const bool pair_tile = p->bm == 256 && p->bn == 256 && (p->grid % 2) == 0;
         if (p->path != GEMM_PATH_TENSOR || (!pair_tile && p->bm != 64 && p->bm != 128) ||
@@ -119,9 +120,20 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     if (!d->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
-    if (skinny)
+    if (skinny) {
+        if (skinny_tc_supported(p->m, p->n, p->k, A, Bt) && tensor_map_encoder_available()) {
+            // as in gemm_i8_run, with the f16 copy of A (m * k * 2 <= 32 MiB for
+            // any k the planner accepts) at the start of the static array
+            if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;
+            uint16_t* A16 = reinterpret_cast<uint16_t*>(d->scratch);
+            if (launch_skinny_prologue(A, A16, C, p->m, p->n, p->k, d->num_sms, stream) != cudaSuccess ||
+                launch_skinny_tc(Bt, A16, C, d->err, p->m, p->n, p->k, d->num_sms, stream) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            return GEMM_OK;
+        }
         return launch_skinny_i8(A, Bt, C, p->m, p->n, p->k, d->num_sms, stream) == cudaSuccess ? GEMM_OK
                                                                                                : GEMM_ERR_CUDA;
+    }
 
     if (!tensor_map_encoder_available()) return GEMM_ERR_CUDA;
     if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;

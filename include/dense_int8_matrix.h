@@ -172,11 +172,11 @@ GEMM_API gemm_status gemm_bf16_run(const gemm_plan *plan, const uint16_t *A, con
  * which every GPU that loads the library holds until the process exits.  The
  * call makes no cudaMalloc, cudaFree or other allocating call.
  *
- * Same arguments, rules and result as gemm_i8_run (the skinny path needs no
- * scratch and runs unchanged).  Extra rules:
+ * Same arguments, rules and result as gemm_i8_run.  Extra rules:
  *   - the tensor-core path needs round256(m*k_pitch*2) + round256(n*k_pitch*2)
  *     bytes of scratch; larger problems return GEMM_ERR_INVALID_ARG and
- *     launch nothing;
+ *     launch nothing; the skinny path needs m*k*2 bytes (at most 32 MiB) for
+ *     the f16 copy of A when k % 16 == 0, and none otherwise;
  *   - the first call on each device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress) and caches it; make that
  *     first call before any stream capture;

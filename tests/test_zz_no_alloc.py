@@ -62,11 +62,20 @@ def test_noalloc_largest_problem_and_rejection():
     assert st == B.GEMM_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("m", [16, 100])
-def test_noalloc_skinny_plan(m):
-    # skinny plans run on CUDA cores here (no scratch); m > 64 in two launches
-    out, ref = _both(m, 4096, 1000, 14 + m)
+@pytest.mark.parametrize("m,k,n", [(16, 4096, 1000), (100, 4096, 1000), (64, 8192, 8192), (8, 1000, 777)])
+def test_noalloc_skinny_plan(m, k, n):
+    # skinny plans: the tensor-core kernel with the f16 copy of A in the static
+    # array (k % 16 == 0), else the CUDA-core kernel, which needs no scratch
+    out, ref = _both(m, k, n, 14 + m)
     assert torch.equal(out, ref)
+
+
+def test_noalloc_skinny_twice_then_tensor():
+    # consecutive calls of both paths through the shared array: stale
+    # contents from the call before would show
+    for m, k, n, seed in [(32, 2048, 3000, 41), (5, 4096, 640, 42), (300, 1024, 500, 43), (16, 1024, 2000, 44)]:
+        out, ref = _both(m, k, n, seed)
+        assert torch.equal(out, ref)
 
 
 @pytest.mark.parametrize("m,k,n", [(512, 8192, 512), (1000, 4096, 300)])
