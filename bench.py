@@ -128,14 +128,21 @@ def load_traffic():
     return out
 
 
-def kernel_source_digest() -> str:
+# the sources each recorded kernel is compiled from (its own file, the PTX
+# helpers and the shared constants)
+KERNEL_SOURCES = {
+    "tc": ("gemm_tc2.cu", "gemm_tc.cu", "ptx.cuh", "internal.h"),
+    "skinny": ("gemm_skinny_tc.cu", "ptx.cuh", "internal.h"),
+}
+
+
+def kernel_source_digest(kind: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_int8_matrix_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in sorted(KERNEL_SOURCES[kind]):
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -413,7 +420,7 @@ def run_ours(args):
                 "algorithmic_flops_per_launch": ops}
         traffic_key = args.workload
     traffic = load_traffic().get(traffic_key)
-    digest = kernel_source_digest()
+    digest = kernel_source_digest("skinny" if skinny else "tc")
     roof["traffic"] = traffic[0] if traffic and traffic[1] == digest else None
     roof["kernel_ms_per_launch"] = per_launch_ms
 
