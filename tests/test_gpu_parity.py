@@ -538,6 +538,37 @@ def test_i8_skinny_chain_direct_alias():
     assert B.gemm_device_error() == (B.GEMM_OK, 0)
 
 
+def test_i8_mixed_paths_chain_direct_alias():
+    # tensor path -> skinny path -> tensor path, back to back on one stream,
+    # each call reading the previous call's C (its bytes) as an operand:
+    #   C1 = A1 Bt1        (256 x 512, tensor path)      512 KiB
+    #   C2 = A2 (C1 as Bt) (8 x 512, skinny path)        16 KiB, Bt = 512 x 1024
+    #   C3 = (C2 as A) Bt3 (256 x 96, tensor path)       A = 256 x 64
+    A1 = workloads.random_i8((256, 512), 341)
+    Bt1 = workloads.random_i8((512, 512), 342)
+    A2 = workloads.random_i8((8, 1024), 343)
+    Bt3 = workloads.random_i8((96, 64), 344)
+    C1 = oracle.gemm_i8(A1.numpy(), Bt1.numpy())
+    C2 = oracle.gemm_i8(A2.numpy(), np.ascontiguousarray(C1).view(np.int8).reshape(512, 1024))
+    C3 = oracle.gemm_i8(np.ascontiguousarray(C2).view(np.int8).reshape(256, 64), Bt3.numpy())
+    p1, p2, p3 = B.gemm_i8_plan(256, 512, 512), B.gemm_i8_plan(8, 1024, 512), B.gemm_i8_plan(256, 64, 96)
+    assert (p1.path, p2.path, p3.path) == (B.GEMM_PATH_TENSOR, B.GEMM_PATH_SKINNY, B.GEMM_PATH_TENSOR)
+    dA1, dB1, dA2, dB3 = A1.cuda(), Bt1.cuda(), A2.cuda(), Bt3.cuda()
+    for rep in range(10):
+        g1 = torch.full((256, 512), -7, dtype=torch.int32, device="cuda")
+        g2 = torch.full((8, 512), -7, dtype=torch.int32, device="cuda")
+        g3 = torch.full((256, 96), -7, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        B.gemm_i8_run(p1, dA1, dB1, g1)
+        B.gemm_i8_run(p2, dA2, g1.view(torch.int8).view(512, 1024), g2)
+        B.gemm_i8_run(p3, g2.view(torch.int8).view(256, 64), dB3, g3)
+        torch.cuda.synchronize()
+        assert np.array_equal(g1.cpu().numpy(), C1)
+        assert np.array_equal(g2.cpu().numpy(), C2), "skinny link, repetition %d" % rep
+        assert np.array_equal(g3.cpu().numpy(), C3), "tensor link, repetition %d" % rep
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
 @pytest.mark.parametrize("m,k,n", [(16, 4096, 1024), (100, 2048, 640)])
 def test_i8_skinny_c_offset(m, k, n):
     # C starting 4 bytes into an allocation (C needs only 4-byte alignment):
