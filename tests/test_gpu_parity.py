@@ -228,6 +228,28 @@ def test_host_entry_points():
     G.assert_bf16_close(Ab, Bb, Cb)
 
 
+@pytest.mark.parametrize("m,k,n,pinned", [(1, 8192, 8192, True), (16, 4096, 4096, False), (100, 2048, 1000, True),
+                                           (8, 1000, 777, False)])
+def test_host_entry_point_skinny(m, k, n, pinned):
+    # skinny plans through the host-buffer form (copies in, prologue and
+    # skinny kernel or the CUDA-core kernel, copy out), three calls in a row
+    # into the same host C
+    A = workloads.random_i8((m, k), 351 + m)
+    Bt = workloads.random_i8((n, k), 352 + m)
+    if pinned:
+        A, Bt = A.pin_memory(), Bt.pin_memory()
+    C = torch.full((m, n), -7, dtype=torch.int32)
+    if pinned:
+        C = C.pin_memory()
+    plan = B.gemm_i8_plan(m, k, n)
+    assert plan.path == B.GEMM_PATH_SKINNY
+    ref = oracle.gemm_i8(A.numpy(), Bt.numpy())
+    for _ in range(3):
+        C.fill_(-7)
+        B.gemm_i8_run_host(plan, A, Bt, C)
+        assert np.array_equal(C.numpy(), ref)
+
+
 @pytest.mark.parametrize("m,k,n,pinned", [(2048, 1024, 2048, True), (3000, 1040, 2800, False), (4096, 4096, 4096, True)])
 def test_host_entry_point_banded(m, k, n, pinned):
     # at least 2048 rows and 32 MiB of copies: the band / rectangle pipeline
