@@ -128,6 +128,9 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
+    // the next kernel in the stream (the next call's staging kernel, which
+    // waits for this one before it touches memory) may launch
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
 
     if (warp == 0 && lane == 0) {

@@ -246,6 +246,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
+    // the next kernel in the stream (the next call's staging kernel, which
+    // waits for this one before it touches memory) may launch
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;

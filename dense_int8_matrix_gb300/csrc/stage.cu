@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kBulkThreads) stage_i8_bulk_kernel(const uint8
                                                                      int64_t a_bytes, int64_t b_bytes,
                                                                      const StageZero z, int* err) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
+    pdl_wait();                // launched ahead of the kernel before: touch nothing until it completes
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sin = base;                                 // kBulkDepth x 8 KiB
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(256) stage_i8_flat_kernel(const uint4* __restr
                                                             uint4* __restrict__ dstB, int64_t itemsA,
                                                             int64_t itemsB, const StageZero z) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
+    pdl_wait();                // launched ahead of the kernel before: touch nothing until it completes
     const int64_t total = itemsA + itemsB;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     zero_work(z, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x, stride);
@@ -244,6 +246,7 @@ __global__ void __launch_bounds__(256) stage_i8_rows_kernel(const int8_t* __rest
                                                             uint4* __restrict__ Bh, int64_t m, int64_t n, int64_t k,
                                                             int64_t k_pitch, const StageZero z) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
+    pdl_wait();                // launched ahead of the kernel before: touch nothing until it completes
     const int64_t cpr = k_pitch / 8;   // 8-element pieces per staged row
     const int64_t itemsA = m * cpr;
     const int64_t total = itemsA + n * cpr;
@@ -272,6 +275,7 @@ __global__ void __launch_bounds__(256) stage_b16_rows_kernel(const uint16_t* __r
                                                              uint4* __restrict__ Ah, uint4* __restrict__ Bh,
                                                              int64_t m, int64_t n, int64_t k, int64_t k_pitch) {
     pdl_launch_dependents();   // the GEMM kernel after this one may start its set-up
+    pdl_wait();                // launched ahead of the kernel before: touch nothing until it completes
     const int64_t cpr = k_pitch / 8;
     const int64_t itemsA = m * cpr;
     const int64_t total = itemsA + n * cpr;
@@ -319,6 +323,27 @@ __global__ void __launch_bounds__(kProThreads, 16) skinny_prologue_kernel(const 
     zero_work(z, t, stride);
 }
 
+// Launch with programmatic stream serialization: the kernel may become
+// resident while the kernel before it in the stream still runs (if that one
+// lets its dependents start early); every staging kernel waits for it
+// (pdl_wait) before touching memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), int grid, int block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+}
+
 int grid_for(int64_t items, int num_sms) {
     // 8 resident 256-thread blocks per SM, grid a multiple of the SM count
     int64_t want = (items + 255) / 256;
@@ -344,21 +369,25 @@ cudaError_t launch_stage_i8(const int8_t* A, const int8_t* Bt, uint16_t* Ah, uin
         // three CTAs per SM (66 KiB of shared memory each)
         const int64_t cap = static_cast<int64_t>(kBulkCtasPerSm) * num_sms;
         const int grid = static_cast<int>(chunks < cap ? chunks : cap);
-        stage_i8_bulk_kernel<<<grid, kBulkThreads, kBulkSmem, stream>>>(
-            reinterpret_cast<const uint8_t*>(A), reinterpret_cast<const uint8_t*>(Bt), reinterpret_cast<uint8_t*>(Ah),
-            reinterpret_cast<uint8_t*>(Bh), m * k, n * k, z, err);
+        e = launch_pdl(stage_i8_bulk_kernel, grid, kBulkThreads, kBulkSmem, stream,
+                       reinterpret_cast<const uint8_t*>(A), reinterpret_cast<const uint8_t*>(Bt),
+                       reinterpret_cast<uint8_t*>(Ah), reinterpret_cast<uint8_t*>(Bh), m * k, n * k, z, err);
+        if (e != cudaSuccess) return e;
     } else if (k == k_pitch && (k % 16) == 0 && aligned) {
         const int64_t itemsA = m * k / 16, itemsB = n * k / 16;
         const int64_t zi = zero_items(z);
         const int64_t work = itemsA + itemsB > zi ? itemsA + itemsB : zi;
-        stage_i8_flat_kernel<<<grid_for(work, num_sms), 256, 0, stream>>>(
-            reinterpret_cast<const uint4*>(A), reinterpret_cast<const uint4*>(Bt), reinterpret_cast<uint4*>(Ah),
-            reinterpret_cast<uint4*>(Bh), itemsA, itemsB, z);
+        cudaError_t e = launch_pdl(stage_i8_flat_kernel, grid_for(work, num_sms), 256, 0, stream,
+                                   reinterpret_cast<const uint4*>(A), reinterpret_cast<const uint4*>(Bt),
+                                   reinterpret_cast<uint4*>(Ah), reinterpret_cast<uint4*>(Bh), itemsA, itemsB, z);
+        if (e != cudaSuccess) return e;
     } else {
         const int64_t items = (m + n) * (k_pitch / 8);
         const int64_t zi = zero_items(z);
-        stage_i8_rows_kernel<<<grid_for(items > zi ? items : zi, num_sms), 256, 0, stream>>>(
-            A, Bt, reinterpret_cast<uint4*>(Ah), reinterpret_cast<uint4*>(Bh), m, n, k, k_pitch, z);
+        cudaError_t e = launch_pdl(stage_i8_rows_kernel, grid_for(items > zi ? items : zi, num_sms), 256, 0, stream,
+                                   A, Bt, reinterpret_cast<uint4*>(Ah), reinterpret_cast<uint4*>(Bh), m, n, k,
+                                   k_pitch, z);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -388,8 +417,9 @@ cudaError_t launch_skinny_prologue(const int8_t* A, uint16_t* A16, int32_t* C, i
 
 cudaError_t launch_stage_b16(const uint16_t* A, const uint16_t* Bt, uint16_t* Ah, uint16_t* Bh, int64_t m,
                              int64_t n, int64_t k, int64_t k_pitch, int num_sms, cudaStream_t stream) {
-    stage_b16_rows_kernel<<<grid_for((m + n) * (k_pitch / 8), num_sms), 256, 0, stream>>>(
-        A, Bt, reinterpret_cast<uint4*>(Ah), reinterpret_cast<uint4*>(Bh), m, n, k, k_pitch);
+    cudaError_t e = launch_pdl(stage_b16_rows_kernel, grid_for((m + n) * (k_pitch / 8), num_sms), 256, 0, stream, A,
+                               Bt, reinterpret_cast<uint4*>(Ah), reinterpret_cast<uint4*>(Bh), m, n, k, k_pitch);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
