@@ -8,11 +8,12 @@ its operands only after its grid dependency wait.  Skinny calls (prologue +
 skinny kernel) and tensor-path calls, with the late write to Bt or to A.
 
 What this can catch, measured on GB300 with copies of the library that had a
-wait removed: the skinny prologue starts while the producer still waits, and
-without its own wait it reads the old A (the A case fails).  The skinny
-kernel behind it did not start before the producer had ended, so the Bt cases
-pin the result but would not catch a missing wait in the skinny kernel; the
-tensor path's staging kernel is an ordinary launch after the producer."""
+wait removed: the skinny prologue and the tensor path's staging kernel start
+while the producer still waits, and without their own wait they read the old
+operand (the skinny A case and both tensor-path cases fail).  The skinny
+kernel behind the prologue did not start before the producer had ended, so
+the skinny Bt cases pin the result but would not catch a missing wait in the
+skinny kernel itself."""
 
 from __future__ import annotations
 
