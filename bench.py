@@ -137,12 +137,19 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_digest(kind: str) -> str:
+    """Digest of the code (comments and blank lines removed) of the sources
+    a recorded kernel is compiled from: an edited comment keeps the record."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_int8_matrix_gb300", "csrc")
     for name in sorted(KERNEL_SOURCES[kind]):
+        text = open(os.path.join(csrc, name), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
         h.update(name.encode())
-        h.update(open(os.path.join(csrc, name), "rb").read())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

@@ -39,10 +39,11 @@
 // Back-to-back calls overlap (programmatic dependent launch): every CTA lets
 // the next kernel in the stream launch as soon as it starts, so the next
 // call's prologue (A to f16, C zeroed: one small CTA per SM beside this one)
-// is resident, waiting, and the next skinny kernel is launched, before this
-// one ends.  Each of its CTAs takes an SM the moment this kernel's CTA there
-// exits and sets up; it loads Bt and its activations and adds into C only
-// after the grid dependency wait.
+// is resident and waiting before this kernel ends.  The skinny kernel behind
+// that prologue launches as this one ends (measured on GB300: only one
+// kernel runs ahead of an unfinished one) and its CTAs take the SMs as they
+// free; each sets up, and loads Bt and its activations and adds into C only
+// after its grid dependency wait.
 //
 // Ring depths, measured on GB300 in back-to-back calls (k = n = 8192): a
 // shallow Bt ring is faster.  A call is bound by the latency of its first
