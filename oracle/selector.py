@@ -1,30 +1,40 @@
 """Oracle for the tile-configuration selector (TEST INFRASTRUCTURE ONLY).
 
-A plain, step-by-step restatement of the five-step method of patent
-CN114238853A ("一種矩陣乘分片配置選擇方法及系統", claim 1 steps 1-5 and claims
-2-6), read for a GPU whose matrix unit is the sm_103a tensor core.  Only the
-tests may import it; the product's planner is separate C++ and shares nothing
-with this file.
+Only the tests may import it; the product's planner is separate C++ and
+shares nothing with this file.  It has two parts, kept apart so that the
+first can be checked against the patent alone:
 
-The patent's formulas did not survive extraction, so each step states the
-reading taken here:
+1. ``five_steps`` restates the five-step method of patent CN114238853A
+   ("一種矩陣乘分片配置選擇方法及系統", claim 1 steps 1-5 and claims 2-6), read
+   for a GPU whose matrix unit is the sm_103a tensor core.  Besides the
+   problem's (m, n) and the SM count, its inputs are the limits of one SM
+   (``Sm``) and the resources each candidate kernel uses (``Candidate``):
+   steps 2 and 5 take a kernel's registers, shared memory and threads as
+   given, and the library's compiled kernels are one such table
+   (``library_candidates``).
+2. The library's own rules, which the pages do not contain: ``route`` sends
+   small-m int8 problems to the skinny path before step 1, and ``k_split``
+   splits small-MN, large-K int8 problems along K after step 5.
 
-Step 1 (claim 1 step 1, claim 2): enumerate the thread-block tiles that the
-    matrix unit can execute.  Tile sides are multiples of the unit's minimum
-    shape ("TCUmin shape size"): BM in {64, 128} (the M of one tensor-core MMA
-    issued by one CTA) and BN in {32, 64, 128, 256}; and the 256 x 256 tile of
-    the two-SM MMA (M = 256), which a pair of thread blocks runs, each with
-    the resources of a (128, 256)-sized CTA.  The K depth of a stage is BK =
-    64 elements of a 16-bit operand (128 bytes, one swizzle row).
-Step 2 (claim 3): drop tiles whose resources do not fit one SM: shared memory
-    of the CTA above the per-CTA limit, or a TMEM accumulator (two buffers of
-    BN columns) above the 512 columns of an SM.
-Step 3 (claim 4 S1-S3): Thread_Blocks = ceil(m/BM) * ceil(n/BN) (the output
-    tiles), twice that for the two-SM tile (two thread blocks per tile);
-    min_theory_block_num = the SM count.  Keep tiles with
-    Thread_Blocks >= min_theory_block_num.  If none qualifies the problem is
-    too small to fill the chip; "set the reuse counts to 1" is read as: keep
-    only the smallest tile, (64, 32).
+``select`` composes them: route, then the five steps, then the K split.
+
+Readings of the five steps (the patent's formulas did not survive
+extraction):
+
+Step 1 (claim 1 step 1, claim 2): the thread-block tiles the matrix unit
+    can execute.  Tile sides are multiples of the unit's minimum shape
+    ("TCUmin shape size"): BM in {64, 128} (the M of one tensor-core MMA
+    issued by one CTA), BN in {32, 64, 128, 256}, and the 256 x 256 tile of
+    the two-SM MMA (M = 256), run by a pair of thread blocks.
+Step 2 (claim 3): drop tiles whose resources do not fit one SM: shared
+    memory of a CTA above the per-CTA limit, or TMEM columns (two
+    accumulators of BN columns) above the SM's.
+Step 3 (claim 4 S1-S3): Thread_Blocks = the CTAs of the output tiling,
+    ceil(m/BM) * ceil(n/BN) tiles times the CTAs per tile;
+    min_theory_block_num = the SM count.  Keep tiles with Thread_Blocks >=
+    min_theory_block_num.  If none qualifies the problem is too small to fill
+    the chip; "set the reuse counts to 1" is read as: keep only the smallest
+    tile.
 Step 4 (claim 5): compute-to-memory ratio of one K step,
     TLP = 2*BM*BN*BK / ((BM + BN)*BK*esize) = 2*BM*BN / ((BM + BN)*esize),
     with the right-matrix tile read as (BK, BN) (the claim's second
@@ -35,61 +45,53 @@ Step 5 (claim 6): block_per_cu = min(registers of an SM // registers of a
     SM // TMEM columns of a CTA); Launch_kernel_times (waves) =
     ceil(Thread_Blocks / (SMs * block_per_cu)).  Keep the fewest waves.
 Tie-break (the pages are silent): larger BM*BN, then larger BM.
-Routing (before step 1, the library's own rule): int8 problems with m <= 64,
-or m <= 128 when k is a multiple of 16, go to the skinny path.
-K split (after step 5, the library's rule for small-MN, large-K problems,
-    where the pages' split-K technique applies: int8 only, since the slices
-    of an int8 product add exactly): when the five steps' choice runs in one
-    wave, the two-SM tile split into S slices along K replaces it if
-    S = min(floor(pairs / T2), floor(k_steps / 16), 8) >= 2, with pairs =
-    floor(SMs / 2), T2 = ceil(m/256) * ceil(n/256) and k_steps = ceil(k/64):
-    every slice keeps at least one 1024-element chunk, and the slices of all
-    tiles run at once.  The plan then has T2 tiles, block_per_cu 1 and
-    ceil(T2 * S / pairs) = 1 wave; "fallback" still records step 3.
 """
 
 from __future__ import annotations
 
 import math
+from dataclasses import dataclass
 
-# Hardware characteristics of one GB300 SM used by steps 2 and 5.
-SMEM_PER_CTA_MAX = 232448       # bytes of shared memory one CTA may use
-SMEM_PER_SM = 233472            # bytes of shared memory per SM
-REGS_PER_SM = 65536             # 32-bit registers per SM
-TMEM_COLS_PER_SM = 512          # TMEM columns (each 128 lanes x 32 bit)
-
-# The candidate kernels: every tile is a CTA of 384 threads with a 4-stage
-# operand ring.  Register use per thread at launch is what the kernel is
-# compiled for: 168 for the wide tiles (BN >= 128, whose epilogue keeps a
-# 64- or 128-entry running sum per thread), 80 for the narrow ones.
-STAGES = 4
-BK_ELEMS = 64
-ESIZE = 2
-THREADS = 384
+BK_ELEMS = 64        # K elements of a 16-bit operand per pipeline stage (128 bytes)
+ESIZE = 2            # bytes per staged operand element (int8 is staged as f16)
 
 
-def regs_per_thread(bn: int) -> int:
-    return 168 if bn >= 128 else 80
+@dataclass(frozen=True)
+class Sm:
+    """Limits of one SM used by steps 2 and 5."""
+    smem_per_cta_max: int = 232448   # bytes of shared memory one CTA may use
+    smem_per_sm: int = 233472        # bytes of shared memory per SM
+    regs_per_sm: int = 65536         # 32-bit registers per SM
+    tmem_cols_per_sm: int = 512      # TMEM columns (each 128 lanes x 32 bit)
 
 
-def is_pair(bm: int, bn: int) -> bool:
-    return bm == 256
+@dataclass(frozen=True)
+class Candidate:
+    """A candidate tile and the resources one CTA of its kernel uses."""
+    bm: int
+    bn: int
+    threads: int
+    regs_per_thread: int
+    smem_bytes: int
+    tmem_cols: int
+    ctas_per_tile: int = 1
 
 
-def smem_per_cta(bm: int, bn: int) -> int:
-    # operand ring + 1 KiB for aligning the ring to the 1024-byte swizzle
-    # atom + 1 KiB for barriers and bookkeeping; wide tiles (BM = 128,
-    # BN >= 128) also stage C for TMA stores in 8 buffers of 4 KiB
-    if is_pair(bm, bn):
-        # each CTA of the pair: 6 stages of 128-row A and B halves
-        return 6 * (128 + 128) * BK_ELEMS * ESIZE + 8 * 4096 + 1024 + 1024
-    epilogue = 8 * 4096 if (bm == 128 and bn >= 128) else 0
-    return STAGES * (bm + bn) * BK_ELEMS * ESIZE + epilogue + 1024 + 1024
+GB300_SM = Sm()
 
 
-def tmem_cols(bn: int) -> int:
-    # two accumulators of BN columns per CTA (each CTA of a 256 x 256 pair
-    # holds two of its 128 x 256 halves: 512 columns)
+# ---------------------------------------------------------------------------
+# The library's compiled kernels as step 1's candidates.  Every one-SM tile is
+# a CTA of 384 threads with a 4-stage operand ring; registers per thread are
+# what the kernel is compiled for (168 for the wide tiles, BN >= 128, whose
+# epilogue keeps 64 or 128 running sums per thread; 80 for the narrow ones);
+# shared memory is the ring + 1 KiB to align it to the 1024-byte swizzle atom
+# + 1 KiB for barriers, plus 8 x 4 KiB of C staging on the wide BM = 128
+# tiles; TMEM is two BN-column accumulators rounded up to a power of two
+# (at least 32).  The two-SM tile: two CTAs per tile, each with a 6-stage ring
+# of 128-row A and B halves, the C staging, and all 512 TMEM columns.
+
+def _tmem_cols(bn: int) -> int:
     need = max(32, 2 * bn)
     cols = 32
     while cols < need:
@@ -97,23 +99,24 @@ def tmem_cols(bn: int) -> int:
     return cols
 
 
-def candidates():
-    """Step 1: every (BM, BN) the tensor core can run as one CTA tile."""
+def library_candidates():
     out = []
     for bm in (64, 128):
         for bn in (32, 64, 128, 256):
-            out.append((bm, bn))
-    out.append((256, 256))
+            epilogue = 8 * 4096 if (bm == 128 and bn >= 128) else 0
+            smem = 4 * (bm + bn) * BK_ELEMS * ESIZE + epilogue + 1024 + 1024
+            out.append(Candidate(bm, bn, 384, 168 if bn >= 128 else 80, smem, _tmem_cols(bn)))
+    out.append(Candidate(256, 256, 384, 168, 6 * (128 + 128) * BK_ELEMS * ESIZE + 8 * 4096 + 1024 + 1024,
+                         512, ctas_per_tile=2))
     return out
 
 
-def fits(bm: int, bn: int) -> bool:
-    """Step 2: resource-fit filter."""
-    if smem_per_cta(bm, bn) > SMEM_PER_CTA_MAX:
-        return False
-    if 2 * bn > TMEM_COLS_PER_SM:
-        return False
-    return True
+# ---------------------------------------------------------------------------
+# The five steps (patent claims 1-6), each a plain function.
+
+def fits(c: Candidate, sm: Sm = GB300_SM) -> bool:
+    """Step 2: the CTA's shared memory and TMEM fit one SM."""
+    return c.smem_bytes <= sm.smem_per_cta_max and c.tmem_cols <= sm.tmem_cols_per_sm
 
 
 def tiles(m: int, n: int, bm: int, bn: int) -> int:
@@ -121,9 +124,9 @@ def tiles(m: int, n: int, bm: int, bn: int) -> int:
     return math.ceil(m / bm) * math.ceil(n / bn)
 
 
-def thread_blocks(m: int, n: int, bm: int, bn: int) -> int:
+def thread_blocks(m: int, n: int, c: Candidate) -> int:
     """Step 3's Thread_Blocks: CTAs over all output tiles."""
-    return tiles(m, n, bm, bn) * (2 if is_pair(bm, bn) else 1)
+    return tiles(m, n, c.bm, c.bn) * c.ctas_per_tile
 
 
 def ratio(bm: int, bn: int) -> float:
@@ -131,75 +134,86 @@ def ratio(bm: int, bn: int) -> float:
     return 2.0 * bm * bn / ((bm + bn) * ESIZE)
 
 
-def blocks_per_sm(bm: int, bn: int) -> int:
+def blocks_per_sm(c: Candidate, sm: Sm = GB300_SM) -> int:
     """Step 5's block_per_cu."""
-    by_regs = REGS_PER_SM // (THREADS * regs_per_thread(bn))
-    by_smem = SMEM_PER_SM // smem_per_cta(bm, bn)
-    by_tmem = TMEM_COLS_PER_SM // tmem_cols(bn)
+    by_regs = sm.regs_per_sm // (c.threads * c.regs_per_thread)
+    by_smem = sm.smem_per_sm // c.smem_bytes
+    by_tmem = sm.tmem_cols_per_sm // c.tmem_cols
     return min(by_regs, by_smem, by_tmem)
 
 
-def waves(m: int, n: int, bm: int, bn: int, num_sms: int) -> int:
+def waves(m: int, n: int, c: Candidate, num_sms: int, sm: Sm = GB300_SM) -> int:
     """Step 5's Launch_kernel_times."""
-    return math.ceil(thread_blocks(m, n, bm, bn) / (num_sms * blocks_per_sm(bm, bn)))
+    return math.ceil(thread_blocks(m, n, c) / (num_sms * blocks_per_sm(c, sm)))
 
 
-def select(dtype: str, m: int, k: int, n: int, num_sms: int) -> dict:
-    """Run the routing and the five steps; return the chosen configuration."""
+def five_steps(m: int, n: int, num_sms: int, candidates=None, sm: Sm = GB300_SM) -> dict:
+    """Patent CN114238853A claim 1 steps 1-5 for an m x n output on
+    `num_sms` SMs; `candidates` defaults to the library's compiled kernels."""
+    cands = list(candidates) if candidates is not None else library_candidates()   # step 1
+    cands = [c for c in cands if fits(c, sm)]                                          # step 2
+    filled = [c for c in cands if thread_blocks(m, n, c) >= num_sms]                  # step 3
+    fallback = not filled
+    cands = filled if filled else [min(cands, key=lambda c: (c.bm * c.bn, c.bm))]
+    best_r = max(ratio(c.bm, c.bn) for c in cands)                                     # step 4
+    cands = [c for c in cands if ratio(c.bm, c.bn) == best_r]
+    best_w = min(waves(m, n, c, num_sms, sm) for c in cands)                           # step 5
+    cands = [c for c in cands if waves(m, n, c, num_sms, sm) == best_w]
+    cands.sort(key=lambda c: (c.bm * c.bn, c.bm), reverse=True)                        # tie-break
+    c = cands[0]
+    return {"bm": c.bm, "bn": c.bn, "tiles": tiles(m, n, c.bm, c.bn), "bpc": blocks_per_sm(c, sm),
+            "waves": best_w, "fallback": fallback}
+
+
+# ---------------------------------------------------------------------------
+# The library's own rules around the five steps (not on the pages).
+
+def route(dtype: str, m: int, k: int) -> str:
+    """Before step 1: int8 problems with m <= 64, or m <= 128 when k is a
+    multiple of 16, take the skinny path (Bt streamed once and widened on
+    chip); every other problem takes the tensor-core path."""
     if dtype not in ("i8", "bf16"):
         raise ValueError(dtype)
     if dtype == "i8" and (m <= 64 or (m <= 128 and k % 16 == 0)):
-        return {"path": "skinny"}
-    # step 1
-    cands = candidates()
-    # step 2
-    cands = [c for c in cands if fits(*c)]
-    # step 3
-    filled = [c for c in cands if thread_blocks(m, n, *c) >= num_sms]
-    fallback = not filled
-    if fallback:
-        cands = [min(cands, key=lambda c: (c[0] * c[1], c[0]))]
-    else:
-        cands = filled
-    # step 4
-    best_r = max(ratio(*c) for c in cands)
-    cands = [c for c in cands if ratio(*c) == best_r]
-    # step 5
-    best_w = min(waves(m, n, *c, num_sms) for c in cands)
-    cands = [c for c in cands if waves(m, n, *c, num_sms) == best_w]
-    # tie-break
-    cands.sort(key=lambda c: (c[0] * c[1], c[0]), reverse=True)
-    bm, bn = cands[0]
-    chosen = {
-        "path": "tensor",
-        "bm": bm,
-        "bn": bn,
-        "tiles": tiles(m, n, bm, bn),
-        "bpc": blocks_per_sm(bm, bn),
-        "waves": best_w,
-        "fallback": fallback,
-        "split": 1,
-    }
-    return k_split(dtype, m, k, n, num_sms, chosen)
+        return "skinny"
+    return "tensor"
 
 
 def k_split(dtype: str, m: int, k: int, n: int, num_sms: int, chosen: dict) -> dict:
-    """The K split after step 5 (see the module docstring)."""
+    """After step 5, int8 only (the slices of an int8 product add exactly):
+    when the five steps' choice runs in one wave, the two-SM tile split into
+    S slices along K replaces it if S = min(floor(pairs / T2),
+    floor(k_steps / 16), 8) >= 2, with pairs = floor(SMs / 2), T2 =
+    ceil(m/256) * ceil(n/256) and k_steps = ceil(k/64): every slice keeps at
+    least one 1024-element chunk, and the slices of all tiles run at once.
+    The plan then has T2 tiles, the two-SM tile's block_per_cu and
+    ceil(T2 * S / pairs) = 1 wave; "fallback" still records step 3."""
+    out = dict(chosen, split=1)
     if dtype != "i8" or chosen["waves"] != 1:
-        return chosen
+        return out
     pairs = num_sms // 2
     t2 = tiles(m, n, 256, 256)
     k_steps = math.ceil(k / BK_ELEMS)
     s = min(pairs // t2, k_steps // 16, 8)
     if s < 2:
-        return chosen
-    return {
-        "path": "tensor",
-        "bm": 256,
-        "bn": 256,
-        "tiles": t2,
-        "bpc": blocks_per_sm(256, 256),
-        "waves": math.ceil(t2 * s / pairs),
-        "fallback": chosen["fallback"],
-        "split": s,
-    }
+        return out
+    pair = [c for c in library_candidates() if c.ctas_per_tile == 2][0]
+    return {"bm": 256, "bn": 256, "tiles": t2, "bpc": blocks_per_sm(pair), "waves": math.ceil(t2 * s / pairs),
+            "fallback": chosen["fallback"], "split": s}
+
+
+def select(dtype: str, m: int, k: int, n: int, num_sms: int) -> dict:
+    """The whole selection the library's planner makes: route, the five
+    steps, the K split."""
+    if route(dtype, m, k) == "skinny":
+        return {"path": "skinny"}
+    chosen = five_steps(m, n, num_sms)
+    return dict(k_split(dtype, m, k, n, num_sms, chosen), path="tensor")
+
+
+# Kept for the tests that look a candidate up by its tile.
+def candidate(bm: int, bn: int) -> Candidate:
+    for c in library_candidates():
+        if (c.bm, c.bn) == (bm, bn):
+            return c
+    raise KeyError((bm, bn))
