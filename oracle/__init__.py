@@ -36,8 +36,9 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + ".tmp%d" % os.getpid()
-    cmd = ["gcc", "-O3", "-std=c11", "-fPIC", "-shared", "-pthread",
-           "-o", tmp, _SRC]
+    # -ffp-contract=off: every float operation is rounded on its own
+    cmd = ["gcc", "-O3", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+           "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -54,8 +55,9 @@ def _load():
     lib.oracle_gemm_bf16.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int]
     lib.oracle_gemm_i8_entries.argtypes = [i64, i64, i64, p, p, i64, p, p, p]
     lib.oracle_gemm_bf16_entries.argtypes = [i64, i64, i64, p, p, i64, p, p, p, p]
+    lib.oracle_requant.argtypes = [i64, i64, p, p, p, ctypes.c_int, p]
     for f in (lib.oracle_gemm_i8, lib.oracle_gemm_bf16,
-              lib.oracle_gemm_i8_entries, lib.oracle_gemm_bf16_entries):
+              lib.oracle_gemm_i8_entries, lib.oracle_gemm_bf16_entries, lib.oracle_requant):
         f.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -149,3 +151,24 @@ def gemm_bf16_entries(A_bits, Bt_bits, rows, cols):
                                           _ptr(rows), _ptr(cols), _ptr(s), _ptr(sa))
     _check(rc)
     return s, sa
+
+
+REQUANT_BF16 = 1
+REQUANT_I8 = 2
+
+
+def requant(C, row_scale, col_scale, out: str):
+    """D = q((float(C) * row_scale[i]) * col_scale[j]) elementwise, every step
+    one binary32 operation rounded to nearest even; q rounds to bfloat16
+    (out = "bf16", returned as uint16 bit patterns) or to int8 with ties to
+    even and saturation (out = "i8")."""
+    C = _as(C, np.int32)
+    rs = _as(row_scale, np.float32)
+    cs = _as(col_scale, np.float32)
+    m, n = C.shape
+    if rs.shape != (m,) or cs.shape != (n,):
+        raise ValueError("scale shapes")
+    kind = {"bf16": REQUANT_BF16, "i8": REQUANT_I8}[out]
+    D = np.empty((m, n), dtype=np.uint16 if kind == REQUANT_BF16 else np.int8)
+    _check(_load().oracle_requant(m, n, _ptr(C), _ptr(rs), _ptr(cs), kind, _ptr(D)))
+    return D

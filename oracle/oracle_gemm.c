@@ -34,11 +34,24 @@
  *
  * Rows of C are split over POSIX threads; each thread owns whole rows, so the
  * arithmetic of every element is the same as in a single-threaded run.
+ *
+ * Requantisation of the exact int32 product (oracle_requant): the usual
+ * consumer of an int8 GEMM scales C per row and per column and stores a
+ * narrower type.  The pages do not define it; the library states it as
+ *
+ *   D[i][j] = q( (float)((float)C[i][j] * row_scale[i]) * col_scale[j] )
+ *
+ * every step one IEEE-754 binary32 operation rounded to nearest, ties to
+ * even: (1) int32 -> float, (2) times the row scale, (3) times the column
+ * scale, (4) q = bfloat16 (round to nearest even; NaN stays NaN; overflow
+ * gives infinity) or int8 (round to the nearest integer, ties to even, then
+ * clamp to [-128, 127]; NaN gives 0).
  */
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 #include <pthread.h>
+#include <math.h>
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG 1
@@ -210,6 +223,70 @@ int oracle_gemm_bf16_entries(int64_t m, int64_t k, int64_t n, const uint16_t *A,
         if (rows[t] < 0 || rows[t] >= m || cols[t] < 0 || cols[t] >= n)
             return ORACLE_ERR_ARG;
         dot_bf16(A + rows[t] * k, Bt + cols[t] * k, k, &sum_out[t], &abs_out[t]);
+    }
+    return ORACLE_OK;
+}
+
+/* ---- requantisation ------------------------------------------------------ */
+
+/* Step 4 for bfloat16: the upper half of the float's bits, rounded to nearest
+ * with ties to even by adding 0x7fff plus the lowest kept bit; NaN -> 0x7fc0. */
+static uint16_t float_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return 0x7fc0;
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* Step 4 for int8: nearest integer, ties to even, then saturation. */
+static int8_t float_to_i8_rne_sat(float z)
+{
+    if (z != z)
+        return 0;
+    float r;
+    if (fabsf(z) >= 8388608.0f) {          /* 2^23: already an integer (or infinite) */
+        r = z;
+    } else {
+        const float fl = floorf(z);
+        const float d = z - fl;            /* exact: z and fl are within 2^23 */
+        if (d > 0.5f)
+            r = fl + 1.0f;
+        else if (d < 0.5f)
+            r = fl;
+        else
+            r = (fmodf(fl, 2.0f) == 0.0f) ? fl : fl + 1.0f;
+    }
+    if (r > 127.0f)
+        return 127;
+    if (r < -128.0f)
+        return -128;
+    return (int8_t)r;
+}
+
+/* D (m x n) from C (m x n int32), row_scale (m), col_scale (n).  out_type 1:
+ * D is bfloat16 (uint16 bit patterns); out_type 2: D is int8. */
+int oracle_requant(int64_t m, int64_t n, const int32_t *C, const float *row_scale,
+                   const float *col_scale, int out_type, void *D)
+{
+    if (m < 0 || n < 0 || (out_type != 1 && out_type != 2))
+        return ORACLE_ERR_ARG;
+    if (m == 0 || n == 0)
+        return ORACLE_OK;
+    if (!C || !row_scale || !col_scale || !D)
+        return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            const float x = (float)C[i * n + j];          /* (1) */
+            const float y = x * row_scale[i];            /* (2) */
+            const float z = y * col_scale[j];            /* (3) */
+            if (out_type == 1)
+                ((uint16_t *)D)[i * n + j] = float_to_bf16_rne(z);   /* (4) */
+            else
+                ((int8_t *)D)[i * n + j] = float_to_i8_rne_sat(z);
+        }
     }
     return ORACLE_OK;
 }

@@ -199,3 +199,95 @@ def test_workload_generators_shapes_and_ranges():
     assert not torch.equal(A, A3)
     A, Bt = workloads.make_inputs("bf16_8192", (4, 64, 8))
     assert A.dtype == torch.bfloat16 and Bt.shape == (8, 64)
+
+
+# ---------------------------------------------------------- requantisation ----
+# D = q((float(C) * row_scale[i]) * col_scale[j]); the expected values below
+# are worked out by hand from the binary32 and bfloat16 formats.
+
+def _rq(oracle_mod, C, rs, cs, out):
+    C = np.asarray(C, np.int32).reshape(len(rs), len(cs))
+    return oracle_mod.requant(C, np.asarray(rs, np.float32), np.asarray(cs, np.float32), out)
+
+
+def test_requant_int8_rounds_half_to_even_and_saturates(oracle_mod):
+    # C * 0.5: 2.5 -> 2, 3.5 -> 4, -2.5 -> -2, -3.5 -> -4, 0.5 -> 0, 1.5 -> 2,
+    # -1.5 -> -2, 9.5 -> 10, -8.5 -> -8; 255.5 rounds to 256 and saturates to
+    # 127, -257 saturates to -128
+    C = [5, 7, -5, -7, 1, 3, -3, 19, -17, 511, -514]
+    got = _rq(oracle_mod, C, [0.5], [1.0] * 11, "i8")
+    want = [2, 4, -2, -4, 0, 2, -2, 10, -8, 127, -128]
+    assert got.tolist() == [want]
+
+
+def test_requant_bf16_ties_to_even(oracle_mod):
+    # 257 lies halfway between the bfloat16 values 256 (0x4380) and 258
+    # (0x4381): the even one, 256; 259 halfway between 258 and 260 (0x4382):
+    # 260; small integers are exact: 1 = 0x3f80, -2 = 0xc000, 3 = 0x4040
+    got = _rq(oracle_mod, [257, 259, -257, 1, -2, 3], [1.0], [1.0] * 6, "bf16")
+    assert got.tolist() == [[0x4380, 0x4382, 0xC380, 0x3F80, 0xC000, 0x4040]]
+
+
+def test_requant_rounds_c_to_float_first(oracle_mod):
+    # 16842753 = 2^24 + 2^16 + 1 is not a float: step (1) rounds it to
+    # 2^24 + 2^16 (even), which is halfway between the bfloat16 values 2^24
+    # (0x4b80) and 2^24 + 2^17 (0x4b81), so bfloat16 rounding gives 0x4b80.
+    # Rounding the integer straight to bfloat16 would give 0x4b81.
+    got = _rq(oracle_mod, [16842753], [1.0], [1.0], "bf16")
+    assert got.tolist() == [[0x4B80]]
+
+
+def test_requant_order_row_scale_then_column_scale(oracle_mod):
+    # C = 2^30, row scale 2^100, column scale 2^-100: step (2) overflows to
+    # infinity, which step (3) keeps (bfloat16 0x7f80, int8 saturates to 127).
+    # Multiplying the two scales first would give exactly 2^30 (0x4e80).
+    rs, cs = [2.0 ** 100], [2.0 ** -100]
+    assert _rq(oracle_mod, [2 ** 30], rs, cs, "bf16").tolist() == [[0x7F80]]
+    assert _rq(oracle_mod, [2 ** 30], rs, cs, "i8").tolist() == [[127]]
+    # and infinity times a zero column scale is NaN: int8 0, bfloat16 NaN
+    assert _rq(oracle_mod, [2 ** 30], rs, [0.0], "i8").tolist() == [[0]]
+    nan = _rq(oracle_mod, [2 ** 30], rs, [0.0], "bf16")[0, 0]
+    assert (nan & 0x7F80) == 0x7F80 and (nan & 0x7F) != 0
+
+
+def test_requant_unit_scales_reproduce_small_integers(oracle_mod):
+    vals = np.arange(-128, 128, dtype=np.int32)
+    got = _rq(oracle_mod, vals, [1.0], [1.0] * 256, "i8")
+    assert np.array_equal(got[0].astype(np.int32), vals)
+
+
+def test_requant_rounding_matches_torch_on_arbitrary_floats(oracle_mod):
+    # with C = 1 and column scale 1, steps (1)-(3) return the row scale x
+    # unchanged, so D = q(x): compare q with torch's own float -> bfloat16
+    # conversion and with torch.round (ties to even) + clamp, on random
+    # finite binary32 bit patterns and on exact bfloat16 ties
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 2 ** 32, size=20000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    ties = (rng.integers(0, 2 ** 16, size=4000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    ties = ties[np.isfinite(ties)]
+    small = (rng.standard_normal(5000) * 200).astype(np.float32)
+    halves = (np.arange(-300, 300, dtype=np.float32) + np.float32(0.5))
+    x = np.concatenate([x, ties, small, halves]).astype(np.float32)
+    C = np.ones((x.size, 1), np.int32)
+    d16 = oracle_mod.requant(C, x, np.ones(1, np.float32), "bf16")[:, 0]
+    ref16 = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(d16, ref16)
+    d8 = oracle_mod.requant(C, x, np.ones(1, np.float32), "i8")[:, 0]
+    ref8 = torch.round(torch.from_numpy(x).double()).clamp(-128, 127).to(torch.int8).numpy()
+    assert np.array_equal(d8, ref8)
+
+
+def test_requant_row_and_column_scales_index_the_right_axis(oracle_mod):
+    # a 2 x 3 case by hand: C = [[10, 20, 30], [-40, 50, -60]],
+    # row scales [0.5, 0.25], column scales [1, 2, 0.1]
+    # row 0: 10*.5*1 = 5, 20*.5*2 = 20, 30*.5 = 15, and 15 times the float
+    #        0.1 (0.100000001490116) is 1.50000002235, which rounds to the
+    #        float 1.5 (spacing 2^-23 there), a tie that rounds to 2
+    # row 1: -40*.25 = -10, 50*.25*2 = 25, -60*.25 = -15 -> -1.5 -> -2
+    C = [[10, 20, 30], [-40, 50, -60]]
+    got = _rq(oracle_mod, C, [0.5, 0.25], [1.0, 2.0, 0.1], "i8")
+    assert got.tolist() == [[5, 20, 2], [-10, 25, -2]]
+    # the transposed roles give a different answer, so a swapped index fails
+    assert got.tolist() != _rq(oracle_mod, C, [1.0, 2.0], [0.5, 0.25, 1.0], "i8").tolist()
