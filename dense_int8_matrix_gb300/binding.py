@@ -29,7 +29,10 @@ GEMM_DTYPE_BF16 = 1
 GEMM_KERNEL_STAGE = 0
 GEMM_KERNEL_TC = 1
 GEMM_KERNEL_SKINNY = 2
-GEMM_KERNEL_KINDS = 3
+GEMM_KERNEL_REQUANT = 3
+GEMM_KERNEL_KINDS = 4
+GEMM_OUT_BF16 = 1
+GEMM_OUT_I8 = 2
 GEMM_PLAN_VERSION = 2
 GEMM_I8_MAX_K = 131071
 GEMM_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -39,7 +42,7 @@ EXPORTED = (
     "gemm_i8_plan", "gemm_bf16_plan", "gemm_plan_for_sms", "gemm_i8_run", "gemm_bf16_run",
     "gemm_i8_run_host", "gemm_bf16_run_host", "gemm_device_error", "gemm_trace_begin",
     "gemm_trace_collect", "gemm_tc_kernel_info", "gemm_selftest_wait_timeout", "gemm_status_string",
-    "gemm_i8_run_noalloc",
+    "gemm_i8_run_noalloc", "gemm_pool_usage", "gemm_i8_run_requant",
 )
 
 
@@ -53,7 +56,7 @@ class gemm_plan(ctypes.Structure):
         ("grid", ctypes.c_int32), ("waves", ctypes.c_int32), ("k_pitch", ctypes.c_int32),
         ("chunk_k", ctypes.c_int32), ("fallback", ctypes.c_int32), ("split_k", ctypes.c_int32),
         ("ratio", ctypes.c_double), ("workspace_bytes", ctypes.c_int64),
-        ("split_from", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("split_from", ctypes.c_int32), ("a_on_chip", ctypes.c_int32),
         ("reserved", ctypes.c_int64 * 3),
     ]
 
@@ -108,6 +111,8 @@ def load():
         "gemm_tc_kernel_info": [i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "gemm_selftest_wait_timeout": [i32, vp],
         "gemm_i8_run_noalloc": [P, vp, vp, vp, vp],
+        "gemm_pool_usage": [ctypes.POINTER(i64), ctypes.POINTER(i64), i32],
+        "gemm_i8_run_requant": [P, vp, vp, vp, vp, i32, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -208,6 +213,20 @@ def gemm_i8_run_noalloc(plan: gemm_plan, A, Bt, C, stream=None) -> None:
     _check(st, "gemm_i8_run_noalloc")
 
 
+def gemm_i8_run_requant(plan: gemm_plan, A, Bt, row_scale, col_scale, D, out_type=None, stream=None) -> None:
+    """D = q((float(A x B) * row_scale[i]) * col_scale[j]) with q = bfloat16
+    (D a torch.bfloat16 tensor) or saturated int8 (D a torch.int8 tensor)."""
+    import torch
+    m, k, n = plan.m, plan.k, plan.n
+    if out_type is None:
+        out_type = GEMM_OUT_BF16 if isinstance(D, torch.Tensor) and D.dtype == torch.bfloat16 else GEMM_OUT_I8
+    d_dtype = torch.bfloat16 if out_type == GEMM_OUT_BF16 else torch.int8
+    st = load().gemm_i8_run_requant(ctypes.byref(plan), _addr(A, torch.int8, (m, k)), _addr(Bt, torch.int8, (n, k)),
+                                    _addr(row_scale, torch.float32, (m,)), _addr(col_scale, torch.float32, (n,)),
+                                    out_type, _addr(D, d_dtype, (m, n)), _stream(stream))
+    _check(st, "gemm_i8_run_requant")
+
+
 def gemm_i8_run_host(plan: gemm_plan, A, Bt, C, stream=None) -> None:
     import torch
     m, k, n = plan.m, plan.k, plan.n
@@ -231,6 +250,16 @@ def gemm_device_error(stream=None):
     code = ctypes.c_int32(0)
     st = load().gemm_device_error(_stream(stream), ctypes.byref(code))
     return st, code.value
+
+
+def gemm_pool_usage(reset_high: bool = False):
+    """(bytes the library's pool holds, most bytes in use at once since the
+    last reset); reset_high restarts the second from the current use."""
+    reserved = ctypes.c_int64(0)
+    high = ctypes.c_int64(0)
+    _check(load().gemm_pool_usage(ctypes.byref(reserved), ctypes.byref(high), 1 if reset_high else 0),
+           "gemm_pool_usage")
+    return reserved.value, high.value
 
 
 def gemm_trace_begin(capacity: int, every: int = 1) -> None:

@@ -52,8 +52,7 @@ gemm_status device_state(DeviceState** out) {
         s.num_sms = sms;
         s.supported = (major == 10 && minor == 3);
         if (s.supported) {
-            if (cudaMalloc(reinterpret_cast<void**>(&s.err_word), sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
-            if (cudaMemset(s.err_word, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+            if (device_error_word(&s.err_word) != cudaSuccess) return GEMM_ERR_CUDA;
             cudaMemPoolProps props;
             std::memset(&props, 0, sizeof(props));
             props.allocType = cudaMemAllocationTypePinned;
@@ -94,6 +93,7 @@ int64_t g_trace_calls = 0;
 int32_t g_trace_launches[GEMM_KERNEL_KINDS] = {};
 std::vector<TraceRec> g_trace;
 size_t g_trace_used = 0;
+size_t g_trace_cap = 0;   // units recorded at most in this trace (g_trace may hold more events)
 
 // Whether this run call is sampled (decided once per call).
 bool trace_sample_call() {
@@ -114,7 +114,7 @@ struct TraceScope {
     TraceScope(int kind, cudaStream_t s, bool sampled) : stream(s) {
         if (!sampled) return;
         std::lock_guard<std::mutex> lock(g_trace_mu);
-        if (g_trace_on && g_trace_used < g_trace.size()) {
+        if (g_trace_on && g_trace_used < g_trace_cap) {
             rec = &g_trace[g_trace_used++];
             rec->kind = kind;
             cudaEventRecord(rec->start, stream);
@@ -126,31 +126,6 @@ struct TraceScope {
 };
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-gemm_status check_plan(const gemm_plan* p, int32_t dtype) {
-    if (!p || p->version != GEMM_PLAN_VERSION || p->dtype != dtype) return GEMM_ERR_INVALID_ARG;
-    if (p->m < 1 || p->k < 1 || p->n < 1) return GEMM_ERR_INVALID_ARG;
-    if (p->path == GEMM_PATH_SKINNY) {
-        if (dtype != GEMM_DTYPE_I8 || p->m > 128 || p->grid < 1) return GEMM_ERR_INVALID_ARG;
-        return GEMM_OK;
-    }
-    if (p->path != GEMM_PATH_TENSOR) return GEMM_ERR_INVALID_ARG;
-    // a plan may be edited to force a tile, but only to one that is compiled
-    if (p->bm == 256) {
-        if (p->bn != 256 || (p->grid % 2) != 0) return GEMM_ERR_INVALID_ARG;
-    } else {
-        if (p->bm != 64 && p->bm != 128) return GEMM_ERR_INVALID_ARG;
-        if (p->bn != 32 && p->bn != 64 && p->bn != 128 && p->bn != 256) return GEMM_ERR_INVALID_ARG;
-    }
-    if (p->grid < 1 || p->k_pitch < p->k || (p->k_pitch % 8) != 0 || p->chunk_k < kTcBK ||
-        (p->chunk_k % kTcBK) != 0)
-        return GEMM_ERR_INVALID_ARG;
-    if (dtype == GEMM_DTYPE_I8 && p->chunk_k > kI8ChunkK) return GEMM_ERR_INVALID_ARG;
-    if (p->split_k < 1 || p->split_k > kTcMaxSplit) return GEMM_ERR_INVALID_ARG;
-    // bf16 problems accumulate the whole K in one TMEM chunk
-    if (dtype == GEMM_DTYPE_BF16 && p->chunk_k < p->k) return GEMM_ERR_INVALID_ARG;
-    return GEMM_OK;
-}
 
 gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* C, cudaStream_t stream) {
     DeviceState* ds = nullptr;
@@ -209,8 +184,10 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     void* ws = nullptr;
     const void* A16 = A;
     const void* B16 = Bt;
+    // int8 A widened inside the two-SM kernel: only Bt is staged
+    const bool a_on_chip = is_i8 && p->a_on_chip == 1;
     if (need_stage) {
-        const int64_t a_bytes = ((p->m * p->k_pitch * 2 + 255) / 256) * 256;
+        const int64_t a_bytes = a_on_chip ? 0 : ((p->m * p->k_pitch * 2 + 255) / 256) * 256;
         const int64_t b_bytes = ((p->n * p->k_pitch * 2 + 255) / 256) * 256;
         if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes), ds->pool, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
@@ -219,7 +196,10 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
         cudaError_t e;
         {
             TraceScope t(GEMM_KERNEL_STAGE, stream, sampled);
-            if (is_i8)
+            if (a_on_chip)
+                e = launch_stage_i8(static_cast<const int8_t*>(Bt), nullptr, Bh, nullptr, p->n, 0, p->k, p->k_pitch,
+                                    z, ds->err_word, ds->num_sms, stream);
+            else if (is_i8)
                 e = launch_stage_i8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(Bt), Ah, Bh, p->m, p->n,
                                     p->k, p->k_pitch, z, ds->err_word, ds->num_sms, stream);
             else
@@ -231,11 +211,12 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
             return GEMM_ERR_CUDA;
         }
         trace_count(GEMM_KERNEL_STAGE);
-        A16 = Ah;
+        A16 = a_on_chip ? nullptr : Ah;
         B16 = Bh;
     }
 
     TcLaunch L;
+    L.A8 = a_on_chip ? A : nullptr;
     L.A16 = A16;
     L.B16 = B16;
     L.C = C;
@@ -262,10 +243,125 @@ gemm_status run_device(const gemm_plan* p, const void* A, const void* Bt, void* 
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-gemm_status check_ptrs(const void* A, const void* Bt, const void* C) {
-    if (!A || !Bt || !C) return GEMM_ERR_INVALID_ARG;
-    if (!aligned(A, 16) || !aligned(Bt, 16) || !aligned(C, 4)) return GEMM_ERR_MISALIGNED;
-    return GEMM_OK;
+// Requantised output: D = q((float(C) * row_scale) * col_scale) with the exact
+// int32 C never written to memory where a CTA completes it.  Whole tensor-path
+// tiles are requantised in the GEMM's epilogue; the tiles of a K split add
+// their int32 partial sums into pool scratch (zeroed by the staging kernel)
+// and the requant kernel converts them afterwards; the skinny path adds into
+// an int32 scratch C, which the requant kernel converts.
+gemm_status run_requant(const gemm_plan* p, const int8_t* A, const int8_t* Bt, const float* rs, const float* cs,
+                        int qmode, void* D, cudaStream_t stream) {
+    DeviceState* ds = nullptr;
+    gemm_status st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    if (!ds->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!tensor_map_encoder_available() && p->path == GEMM_PATH_TENSOR) return GEMM_ERR_CUDA;
+    const int64_t m = p->m, n = p->n, k = p->k;
+    auto al = [](int64_t b) { return static_cast<size_t>((b + 255) / 256 * 256); };
+    RqOut o;
+    o.D = D;
+    o.row_scale = rs;
+    o.col_scale = cs;
+    o.ldd = n;
+    o.qmode = qmode;
+    const uintptr_t dp = reinterpret_cast<uintptr_t>(D);
+    o.d_vec = qmode == kQuantBf16 ? ((dp % 16) == 0 && (n * 2) % 16 == 0) : ((dp % 8) == 0 && n % 8 == 0);
+    const size_t c_bytes = al(m * n * 4);
+    const bool sampled = trace_sample_call();
+
+    if (p->path == GEMM_PATH_SKINNY) {
+        const bool tc = skinny_tc_supported(m, n, k, A, Bt) && tensor_map_encoder_available();
+        const size_t a16 = tc ? al(m * k * 2) : 0;
+        void* ws = nullptr;
+        if (cudaMallocFromPoolAsync(&ws, c_bytes + a16, ds->pool, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        int32_t* C32 = static_cast<int32_t*>(ws);
+        cudaError_t e;
+        {
+            TraceScope t(GEMM_KERNEL_SKINNY, stream, sampled);
+            if (tc) {
+                uint16_t* A16 = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + c_bytes);
+                e = launch_skinny_prologue(A, A16, C32, m, n, k, ds->num_sms, stream);
+                if (e == cudaSuccess) {
+                    trace_count(GEMM_KERNEL_STAGE);
+                    e = launch_skinny_tc(Bt, A16, C32, ds->err_word, m, n, k, ds->num_sms, stream);
+                }
+            } else {
+                e = launch_skinny_i8(A, Bt, C32, m, n, k, ds->num_sms, stream);
+            }
+            if (e == cudaSuccess) trace_count(GEMM_KERNEL_SKINNY);
+        }
+        if (e == cudaSuccess) {
+            TraceScope t(GEMM_KERNEL_REQUANT, stream, sampled);
+            e = launch_requant(C32, n, o, m, n, RqTiles{}, ds->num_sms, stream);
+            if (e == cudaSuccess) trace_count(GEMM_KERNEL_REQUANT);
+        }
+        cudaFreeAsync(ws, stream);
+        return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+
+    const int chunk_kb = p->chunk_k / kTcBK;
+    int64_t split_from = 0;
+    StageZero z;
+    const int split = tc_launch_split(nullptr, m, n, k, p->bm, p->bn, p->grid, chunk_kb, true, ds->tc2_pairs,
+                                      p->split_from == 0 ? p->split_k : 1, &split_from, &z);
+    const int64_t tiles_m = (m + p->bm - 1) / p->bm, tiles_n = (n + p->bn - 1) / p->bn;
+    const bool a_on_chip = p->a_on_chip == 1;   // int8 A widened inside the two-SM kernel
+    const size_t a_bytes = a_on_chip ? 0 : al(m * p->k_pitch * 2), b_bytes = al(n * p->k_pitch * 2);
+    const bool need_c = split > 1;   // int32 scratch for the split tiles' partial sums
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, a_bytes + b_bytes + (need_c ? c_bytes : 0), ds->pool, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    uint16_t* Ah = static_cast<uint16_t*>(ws);
+    uint16_t* Bh = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + a_bytes);
+    int32_t* C32 = need_c ? reinterpret_cast<int32_t*>(static_cast<char*>(ws) + a_bytes + b_bytes) : nullptr;
+    z.C = C32;
+    cudaError_t e;
+    {
+        TraceScope t(GEMM_KERNEL_STAGE, stream, sampled);
+        e = a_on_chip ? launch_stage_i8(Bt, nullptr, Bh, nullptr, n, 0, k, p->k_pitch, z, ds->err_word, ds->num_sms,
+                                        stream)
+                      : launch_stage_i8(A, Bt, Ah, Bh, m, n, k, p->k_pitch, z, ds->err_word, ds->num_sms, stream);
+    }
+    if (e == cudaSuccess) {
+        trace_count(GEMM_KERNEL_STAGE);
+        TcLaunch L;
+        L.A8 = a_on_chip ? A : nullptr;
+        L.A16 = a_on_chip ? nullptr : Ah;
+        L.B16 = Bh;
+        L.C = C32;
+        L.err = ds->err_word;
+        L.m = m;
+        L.n = n;
+        L.k = k;
+        L.k_pitch = p->k_pitch;
+        L.bm = p->bm;
+        L.bn = p->bn;
+        L.grid = p->grid;
+        L.chunk_kb = chunk_kb;
+        L.int_out = true;
+        L.split_k = split;
+        L.split_from = split_from;
+        L.rq = o;
+        {
+            TraceScope t(GEMM_KERNEL_TC, stream, sampled);
+            e = p->bm == 256 ? launch_tc2(L, ds->tc2_pairs, stream) : launch_tc(L, stream);
+        }
+        if (e == cudaSuccess) trace_count(GEMM_KERNEL_TC);
+    }
+    if (e == cudaSuccess && need_c) {
+        RqTiles tl;
+        tl.bm = p->bm;
+        tl.bn = p->bn;
+        tl.tiles_m = static_cast<int>(tiles_m);
+        tl.tiles_n = static_cast<int>(tiles_n);
+        tl.tile_from = static_cast<int>(split_from);
+        tl.tile_to = static_cast<int>(tiles_m * tiles_n);
+        TraceScope t(GEMM_KERNEL_REQUANT, stream, sampled);
+        e = launch_requant(C32, n, o, m, n, tl, ds->num_sms, stream);
+        if (e == cudaSuccess) trace_count(GEMM_KERNEL_REQUANT);
+    }
+    cudaFreeAsync(ws, stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 // The end-to-end form is bound by the host link (about 200 GB/s each way on
@@ -522,6 +618,41 @@ gemm_status run_host(const gemm_plan* p, int32_t dtype, const void* A, const voi
 
 }  // namespace
 
+// Argument checks shared with the allocation-free entry point (noalloc.cu).
+gemm_status gemm::check_plan(const gemm_plan* p, int32_t dtype) {
+    if (!p || p->version != GEMM_PLAN_VERSION || p->dtype != dtype) return GEMM_ERR_INVALID_ARG;
+    if (p->m < 1 || p->k < 1 || p->n < 1) return GEMM_ERR_INVALID_ARG;
+    if (p->path == GEMM_PATH_SKINNY) {
+        if (dtype != GEMM_DTYPE_I8 || p->m > 128 || p->grid < 1) return GEMM_ERR_INVALID_ARG;
+        return GEMM_OK;
+    }
+    if (p->path != GEMM_PATH_TENSOR) return GEMM_ERR_INVALID_ARG;
+    // a plan may be edited to force a tile, but only to one that is compiled
+    if (p->bm == 256) {
+        if (p->bn != 256 || (p->grid % 2) != 0) return GEMM_ERR_INVALID_ARG;
+    } else {
+        if (p->bm != 64 && p->bm != 128) return GEMM_ERR_INVALID_ARG;
+        if (p->bn != 32 && p->bn != 64 && p->bn != 128 && p->bn != 256) return GEMM_ERR_INVALID_ARG;
+    }
+    if (p->grid < 1 || p->k_pitch < p->k || (p->k_pitch % 8) != 0 || p->chunk_k < kTcBK ||
+        (p->chunk_k % kTcBK) != 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (dtype == GEMM_DTYPE_I8 && p->chunk_k > kI8ChunkK) return GEMM_ERR_INVALID_ARG;
+    if (p->split_k < 1 || p->split_k > kTcMaxSplit) return GEMM_ERR_INVALID_ARG;
+    // A widened on chip: the two-SM kernel, int8, a 16-byte row pitch of int8 A
+    if (p->a_on_chip != 0 && (p->a_on_chip != 1 || dtype != GEMM_DTYPE_I8 || p->bm != 256 || (p->k % 16) != 0))
+        return GEMM_ERR_INVALID_ARG;
+    // bf16 problems accumulate the whole K in one TMEM chunk
+    if (dtype == GEMM_DTYPE_BF16 && p->chunk_k < p->k) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+gemm_status gemm::check_ptrs(const void* A, const void* Bt, const void* C) {
+    if (!A || !Bt || !C) return GEMM_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(Bt, 16) || !aligned(C, 4)) return GEMM_ERR_MISALIGNED;
+    return GEMM_OK;
+}
+
 cudaError_t gemm::kernel_attrs_once(const void* kern, int smem_bytes, bool max_carveout) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -579,6 +710,19 @@ gemm_status gemm_bf16_run(const gemm_plan* plan, const uint16_t* A, const uint16
     return run_device(plan, A, Bt, C, static_cast<cudaStream_t>(stream));
 }
 
+gemm_status gemm_i8_run_requant(const gemm_plan* plan, const int8_t* A, const int8_t* Bt, const float* row_scale,
+                                const float* col_scale, int32_t out_type, void* D, void* stream) {
+    gemm_status st = check_plan(plan, GEMM_DTYPE_I8);
+    if (st != GEMM_OK) return st;
+    if (out_type != GEMM_OUT_BF16 && out_type != GEMM_OUT_I8) return GEMM_ERR_INVALID_ARG;
+    if (!A || !Bt || !D || !row_scale || !col_scale) return GEMM_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(Bt, 16) || !aligned(row_scale, 16) || !aligned(col_scale, 16) ||
+        (out_type == GEMM_OUT_BF16 && !aligned(D, 2)))
+        return GEMM_ERR_MISALIGNED;
+    return run_requant(plan, A, Bt, row_scale, col_scale, out_type == GEMM_OUT_BF16 ? kQuantBf16 : kQuantI8, D,
+                       static_cast<cudaStream_t>(stream));
+}
+
 gemm_status gemm_i8_run_host(const gemm_plan* plan, const int8_t* A, const int8_t* Bt, int32_t* C, void* stream) {
     return run_host(plan, GEMM_DTYPE_I8, A, Bt, C, static_cast<cudaStream_t>(stream));
 }
@@ -603,6 +747,25 @@ gemm_status gemm_device_error(void* stream, int32_t* code) {
     return GEMM_ERR_TIMEOUT;
 }
 
+gemm_status gemm_pool_usage(int64_t* reserved_bytes, int64_t* used_high_bytes, int32_t reset_high) {
+    if (!reserved_bytes || !used_high_bytes) return GEMM_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    gemm_status st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    if (!ds->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    uint64_t reserved = 0, high = 0;
+    if (cudaMemPoolGetAttribute(ds->pool, cudaMemPoolAttrReservedMemCurrent, &reserved) != cudaSuccess ||
+        cudaMemPoolGetAttribute(ds->pool, cudaMemPoolAttrUsedMemHigh, &high) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    *reserved_bytes = static_cast<int64_t>(reserved);
+    *used_high_bytes = static_cast<int64_t>(high);
+    if (reset_high) {
+        uint64_t zero = 0;   // the high-water mark restarts from the current use
+        if (cudaMemPoolSetAttribute(ds->pool, cudaMemPoolAttrUsedMemHigh, &zero) != cudaSuccess) return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
 gemm_status gemm_trace_begin(int32_t capacity, int32_t every) {
     if (capacity < 0 || every < 1) return GEMM_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_trace_mu);
@@ -617,6 +780,7 @@ gemm_status gemm_trace_begin(int32_t capacity, int32_t every) {
         g_trace.push_back(r);
     }
     g_trace_used = 0;
+    g_trace_cap = static_cast<size_t>(capacity);
     g_trace_every = every;
     g_trace_calls = 0;
     for (int i = 0; i < GEMM_KERNEL_KINDS; ++i) g_trace_launches[i] = 0;

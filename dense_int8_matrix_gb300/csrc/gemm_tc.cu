@@ -35,6 +35,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "requant.cuh"
 
 namespace gemm {
 
@@ -66,6 +67,7 @@ struct TcParams {
     int num_kb;     // ceil(k / 64)
     int chunk_kb;   // K steps per accumulator chunk
     int tiles_m, tiles_n, tiles;
+    RqOut rq;       // qmode != none: whole tiles requantised into rq.D, not written to C
     int units;      // split_from + (tiles - split_from) * split_k
     int split_from; // tiles [split_from, tiles) run as split_k K slices each (C zeroed over them)
     int split_k;
@@ -307,6 +309,23 @@ __global__ void __launch_bounds__(kTcThreads, (BN >= 128 ? 1 : 2))
                     // fp32 values as loaded
 #define GEMM_TC_OUT(j) (INT_OUT ? static_cast<uint32_t>(acc[(INT_OUT ? sl * Cfg::SLICE : 0) + (j)]) : r[INT_OUT ? 0 : (j)])
                     const int64_t cs = col0 + sl * Cfg::SLICE;
+                    if constexpr (INT_OUT) {
+                        if (p.rq.qmode != kQuantNone && !add_into) {
+                            // a whole tile: its exact sums are final, requantise
+                            // them straight into D (eight columns per store)
+                            if (row_valid) {
+                                const float rs = row < p.m ? __ldg(p.rq.row_scale + row) : 0.f;
+#pragma unroll
+                                for (int g = 0; g < Cfg::SLICE / 8; ++g) {
+                                    int32_t t[8];
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j) t[j] = acc[sl * Cfg::SLICE + g * 8 + j];
+                                    requant_store8(p.rq, p.m, p.n, row, cs + g * 8, rs, t);
+                                }
+                            }
+                            continue;
+                        }
+                    }
                     if constexpr (C_TMA) {
                         // Coalesced write-back (the shared-memory staged epilogue of
                         // "先导杯比赛回顾", section "Epilogue 写回优化"): each lane writes
@@ -465,7 +484,13 @@ cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     int c_tma = 0;
     const int64_t ldc = a.ldc > 0 ? a.ldc : a.n;
     if (ldc < a.n) return cudaErrorInvalidValue;
-    if (Cfg::TMA_STORE && (ldc % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0) {
+    // C may be absent only when every tile is requantised into rq.D
+    const bool split = INT_OUT && a.split_k > 1;
+    const bool requant = INT_OUT && a.rq.qmode != kQuantNone;
+    if (a.C == nullptr && (!requant || split)) return cudaErrorInvalidValue;
+    if (requant && (a.rq.D == nullptr || a.rq.row_scale == nullptr || a.rq.col_scale == nullptr))
+        return cudaErrorInvalidValue;
+    if (Cfg::TMA_STORE && a.C != nullptr && (ldc % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0) {
         if (!encode_c_map(&mC, a.C, a.m, a.n, ldc)) return cudaErrorInvalidValue;
         c_tma = 1;
     }
@@ -484,6 +509,7 @@ cudaError_t launch_one(const TcLaunch& a, cudaStream_t stream) {
     p.split_k = a.split_k > 1 ? a.split_k : 1;
     p.split_from = p.split_k > 1 ? static_cast<int>(a.split_from) : p.tiles;
     p.units = p.split_from + (p.tiles - p.split_from) * p.split_k;
+    p.rq = requant ? a.rq : RqOut{};
     auto kern = c_tma ? gemm_tc_kernel<BM, BN, INT_OUT, Cfg::TMA_STORE> : gemm_tc_kernel<BM, BN, INT_OUT, false>;
     cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;

@@ -24,6 +24,14 @@
 //               TMA-store or vector-store C); releases the accumulator on the
 //               even CTA's barrier.
 //
+// Widened A (int8 problems with k % 16 == 0, chosen by the caller for narrow
+// C, where a staged f16 copy of A would cost more traffic than the multiply):
+// int8 A is loaded by TMA (128 rows x 64 bytes per K step) into a separate
+// ring, and warps 2-3 of each CTA widen it exactly to f16 in the 128-byte
+// swizzled layout of the operand ring, so A crosses HBM once, as int8; Bt
+// still comes from the staged f16 copy.  The widened halves of both CTAs are
+// announced on the even CTA's "full" barrier beside the TMA bytes of Bt.
+//
 // Tail split (int8 problems): when the last round of pairs is only partly
 // filled, the tiles of that round run as split_k K slices on otherwise idle
 // pairs.  The staging kernel zeroes C over those tiles, and every slice adds
@@ -37,6 +45,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "requant.cuh"
 
 namespace gemm {
 
@@ -52,6 +61,22 @@ constexpr int kT2EpiBytes = kTcEpilogueWarps * kTcEpiStageBytes;
 constexpr size_t kT2Smem = static_cast<size_t>(kT2Stages) * kT2StageBytes + kT2EpiBytes + 1024 + 1024;
 static_assert(kT2Smem == tc2_smem_bytes(), "shared-memory size known to the planner");
 
+// Widened-A variant: a 5-stage f16 operand ring and a 4-stage ring of int8 A
+// (128 rows x 64 bytes = 8 KiB per stage and CTA).
+constexpr int kT2WStages = 5;
+constexpr int kT2W8Stages = 4;
+constexpr int kT2W8Bytes = kT2Half * kTcBK;        // 8 KiB
+constexpr int kT2WidenThreads = 64;                // warps 2 and 3
+constexpr size_t kT2WSmem = static_cast<size_t>(kT2WStages) * kT2StageBytes +
+                            static_cast<size_t>(kT2W8Stages) * kT2W8Bytes + kT2EpiBytes + 1024 + 1024;
+static_assert(kT2WSmem <= 232448, "widened-A shared memory");
+
+template <bool WIDEN_A>
+struct T2Ring {
+    static constexpr int STAGES = WIDEN_A ? kT2WStages : kT2Stages;
+    static constexpr size_t SMEM = WIDEN_A ? kT2WSmem : kT2Smem;
+};
+
 struct T2Params {
     void* C;
     int* err;
@@ -63,6 +88,7 @@ struct T2Params {
     int units;                     // split_from + (tiles - split_from) * split_k
     int split_from;                // tiles [split_from, tiles) run as split_k K slices (C zeroed over them)
     int split_k;
+    RqOut rq;                      // qmode != none: whole tiles requantised into rq.D, not written to C
 };
 
 // A unit of work: one tile over the K steps [kb_lo, kb_hi).  Units below
@@ -145,6 +171,31 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
         : "memory");
 }
 
+// Named barrier 1 of the two widening warps (64 threads).
+__device__ __forceinline__ void widen_group_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// The same barrier, returning whether `pred` holds in every thread of the
+// group, so that both warps leave their loop together or not at all.
+__device__ __forceinline__ bool widen_group_all(int pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred)
+        : "memory");
+    return r != 0;
+}
+
+// Arrive on a barrier given by its shared::cluster address with the default
+// (CTA-scope) release: the widening group's hand-off to the even CTA's MMA
+// issuer, which then waits with the default acquire.  The widened bytes sit
+// in the arriving CTA's own shared memory and are read there by its SM's half
+// of the pair MMA; fence.proxy.async before the arrival orders them for the
+// tensor core.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // Arrive on a barrier given by its shared::cluster address (possibly remote).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
@@ -225,24 +276,29 @@ __device__ __forceinline__ void store_slice32(const CUtensorMap* tmC, const T2Pa
     }
 }
 
-template <bool INT_OUT, bool C_TMA>
+template <bool INT_OUT, bool C_TMA, bool WIDEN_A>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const T2Params p) {
+    static_assert(!WIDEN_A || INT_OUT, "A is widened from int8 only");
+    constexpr int kStages = T2Ring<WIDEN_A>::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sA = base;
-    const uint32_t sB = base + kT2Stages * kT2HalfBytes;
-    const uint32_t sEpi = base + kT2Stages * kT2StageBytes;
-    uint8_t* ctrl = smem_raw + (base - raw) + kT2Stages * kT2StageBytes + kT2EpiBytes;
+    const uint32_t sB = base + kStages * kT2HalfBytes;
+    const uint32_t sA8 = base + kStages * kT2StageBytes;   // int8 A ring (widened-A variant)
+    const uint32_t sEpi = sA8 + (WIDEN_A ? kT2W8Stages * kT2W8Bytes : 0);
+    uint8_t* ctrl = smem_raw + (sEpi - raw) + kT2EpiBytes;
     const uint32_t bar0 = smem_u32(ctrl);
     const uint32_t full_bar0 = bar0;                        // used in the even CTA
-    const uint32_t empty_bar0 = bar0 + 8u * kT2Stages;
-    const uint32_t accf_bar0 = bar0 + 16u * kT2Stages;
+    const uint32_t empty_bar0 = bar0 + 8u * kStages;
+    const uint32_t accf_bar0 = bar0 + 16u * kStages;
     const uint32_t acce_bar0 = accf_bar0 + 16u;             // used in the even CTA
     const uint32_t done_bar = acce_bar0 + 16u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kT2Stages + 5));
+    const uint32_t a8full_bar0 = done_bar + 8u;             // [kT2W8Stages] int8 A landed (local)
+    const uint32_t a8empty_bar0 = a8full_bar0 + 8u * kT2W8Stages;   // [kT2W8Stages] int8 A read (local)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kStages + 5 + 2 * kT2W8Stages));
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -256,8 +312,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int npairs = gridDim.x >> 1;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < kT2Stages; ++s) {
-            mbar_init(full_bar0 + 8u * s, 1);
+        for (int s = 0; s < kStages; ++s) {
+            // widened A: the producer's arrival plus one per CTA's widening group
+            mbar_init(full_bar0 + 8u * s, WIDEN_A ? 3 : 1);
             mbar_init(empty_bar0 + 8u * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -265,6 +322,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(acce_bar0 + 8u * b, 2 * kTcEpilogueWarps);
         }
         mbar_init(done_bar, 1);
+        if constexpr (WIDEN_A) {
+            for (int s = 0; s < kT2W8Stages; ++s) {
+                mbar_init(a8full_bar0 + 8u * s, 1);
+                mbar_init(a8empty_bar0 + 8u * s, 1);
+            }
+        }
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -289,20 +352,95 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int ya = w.tm * 256 + static_cast<int>(rank) * kT2Half;
                 const int yb = w.tn * 256 + static_cast<int>(rank) * kT2Half;
                 for (int kb = w.kb_lo; kb < w.kb_hi; ++kb) {
-                    const uint32_t s = issued % kT2Stages;
-                    const uint32_t ph = (issued / kT2Stages) & 1u;
+                    const uint32_t s = issued % kStages;
+                    const uint32_t ph = (issued / kStages) & 1u;
                     if (!wait_bounded(empty_bar0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) {
                         ok = false;
                         break;
                     }
-                    // both CTAs' copies complete on the even CTA's barrier,
-                    // which expects the bytes of both
-                    if (leader) mbar_arrive_expect_tx(full_bar0 + 8u * s, 2 * kT2StageBytes);
                     const uint32_t fb = map_to_rank(full_bar0 + 8u * s, 0);
-                    tma_load_2d_pair(sA + s * kT2HalfBytes, &tmA, kb * kTcBK, ya, fb, pol);
+                    if constexpr (WIDEN_A) {
+                        // int8 A into its own ring (local barrier); only the
+                        // bytes of Bt complete on the even CTA's barrier
+                        const uint32_t s8 = issued % kT2W8Stages, ph8 = (issued / kT2W8Stages) & 1u;
+                        if (!wait_bounded(a8empty_bar0 + 8u * s8, ph8 ^ 1u, abort_flag, p.err,
+                                          kDevErrTimeoutProducer)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(a8full_bar0 + 8u * s8, kT2W8Bytes);
+                        tma_load_2d(sA8 + s8 * kT2W8Bytes, &tmA, kb * kTcBK, ya, a8full_bar0 + 8u * s8, pol);
+                        if (leader) mbar_arrive_expect_tx(full_bar0 + 8u * s, 2 * kT2HalfBytes);
+                    } else {
+                        // both CTAs' copies complete on the even CTA's barrier,
+                        // which expects the bytes of both
+                        if (leader) mbar_arrive_expect_tx(full_bar0 + 8u * s, 2 * kT2StageBytes);
+                        tma_load_2d_pair(sA + s * kT2HalfBytes, &tmA, kb * kTcBK, ya, fb, pol);
+                    }
                     tma_load_2d_pair(sB + s * kT2HalfBytes, &tmB, kb * kTcBK, yb, fb, pol);
                     ++issued;
                 }
+            }
+            if constexpr (WIDEN_A) {
+                // Teardown: the int8 copies still in flight must land before
+                // the CTA exits (earlier ones were waited for by the widening
+                // group before their slot was reused)
+                for (uint32_t j = issued > static_cast<uint32_t>(kT2W8Stages) ? issued - kT2W8Stages : 0u;
+                     j < issued; ++j)
+                    wait_bounded(a8full_bar0 + 8u * (j % kT2W8Stages), (j / kT2W8Stages) & 1u, nullptr, p.err,
+                                 kDevErrTimeoutTeardown);
+            }
+        }
+    } else if (WIDEN_A && (warp == 2 || warp == 3)) {
+        // --------------------------------------------- widen int8 A to f16 --
+        // Per K step: 128 rows x 64 int8 (512 chunks of 16 bytes, eight per
+        // thread) -> 128 rows x 64 f16 in the 128-byte swizzled layout the
+        // MMA descriptor reads (chunk c of row r at ((c ^ (r & 7)) << 4)).
+        const int t = threadIdx.x - 64;   // 0..63
+        uint32_t done = 0;
+        bool ok = true;
+        const uint32_t fb = map_to_rank(full_bar0, 0);
+        for (int u = pair; ok && u < p.units; u += npairs) {
+            const Unit2 w = unit_at2(u, p);
+            for (int kb = w.kb_lo; kb < w.kb_hi; ++kb) {
+                const uint32_t s = done % kStages, ph = (done / kStages) & 1u;
+                const uint32_t s8 = done % kT2W8Stages, ph8 = (done / kT2W8Stages) & 1u;
+                int got = 1;
+                if (lane == 0)
+                    got = (wait_bounded(a8full_bar0 + 8u * s8, ph8, abort_flag, p.err, kDevErrTimeoutProducer) &&
+                           wait_bounded(empty_bar0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer))
+                              ? 1
+                              : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!widen_group_all(got)) {   // both warps leave together
+                    ok = false;
+                    break;
+                }
+                const uint32_t src = sA8 + s8 * kT2W8Bytes;
+                const uint32_t dst = sA + s * kT2HalfBytes;
+                // all eight loads first (the shared-memory accesses are
+                // volatile asm, which the compiler keeps in program order),
+                // then widen and store
+                uint4 v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = ld_shared_v4(src + (t + kT2WidenThreads * i) * 16);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int q = t + kT2WidenThreads * i;   // 16-byte int8 chunk: row q / 4, chunk q % 4
+                    const int r = q >> 2, c = q & 3;
+                    uint32_t wv[8];
+                    widen16(v[i], wv);
+                    const uint32_t row = dst + r * 128;
+                    st_shared_v4(row + (((2 * c) ^ (r & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
+                    st_shared_v4(row + (((2 * c + 1) ^ (r & 7)) << 4), wv[4], wv[5], wv[6], wv[7]);
+                }
+                fence_proxy_async_smem();   // the MMA (async proxy) reads what was just written
+                widen_group_sync();
+                if (t == 0) {
+                    mbar_arrive(a8empty_bar0 + 8u * s8);
+                    mbar_arrive_remote(fb + 8u * s);
+                }
+                ++done;
             }
         }
     } else if (warp == 1) {
@@ -324,8 +462,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t d_tmem = tmem_base + buf * kT2Cols;
                     const int c1 = min(w.kb_hi, c0 + p.chunk_kb);
                     for (int kb = c0; kb < c1; ++kb) {
-                        const uint32_t s = consumed % kT2Stages;
-                        const uint32_t ph = (consumed / kT2Stages) & 1u;
+                        const uint32_t s = consumed % kStages;
+                        const uint32_t ph = (consumed / kStages) & 1u;
                         if (!wait_bounded(full_bar0 + 8u * s, ph, abort_flag, p.err, kDevErrTimeoutMma)) {
                             ok = false;
                             break;
@@ -403,6 +541,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) mbar_arrive_cluster(acce_leader + 8u * buf);
                     ++acc_iter;
                     if (!last) continue;
+                    if (p.rq.qmode != kQuantNone && w.split_tile < 0) {
+                        // a whole tile: its exact sums are final, requantise them
+                        // straight into D (eight columns per store)
+                        const float rs = row < p.m ? __ldg(p.rq.row_scale + row) : 0.f;
+#pragma unroll
+                        for (int g = 0; g < kT2Half2 / 8; ++g) {
+                            int32_t t[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) t[j] = acc[g * 8 + j];
+                            requant_store8(p.rq, p.m, p.n, row, col0 + g * 8, rs, t);
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int sl = 0; sl < kT2Half2 / 32; ++sl) {
                         uint32_t r[32];
@@ -454,12 +605,28 @@ bool encode(CUtensorMap* map, CUtensorMapDataType type, void* ptr, uint64_t inne
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool INT_OUT, bool C_TMA>
+template <bool INT_OUT, bool C_TMA, bool WIDEN_A = false>
 const void* tc2_kernel_ptr() {
-    return reinterpret_cast<const void*>(gemm_tc2_kernel<INT_OUT, C_TMA>);
+    return reinterpret_cast<const void*>(gemm_tc2_kernel<INT_OUT, C_TMA, WIDEN_A>);
 }
 
-cudaError_t configure2(const void* kern) { return kernel_attrs_once(kern, static_cast<int>(kT2Smem), true); }
+cudaError_t configure2(const void* kern, size_t smem = kT2Smem) {
+    return kernel_attrs_once(kern, static_cast<int>(smem), true);
+}
+
+// int8 A, m x k row-major (k % 16 == 0): 64-byte x 128-row boxes, no swizzle;
+// rows and K beyond the matrix read as zero.
+bool encode_a8(CUtensorMap* map, const void* ptr, uint64_t k, uint64_t m) {
+    auto enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!enc) return false;
+    cuuint64_t dims[2] = {k, m};
+    cuuint64_t strides[1] = {k};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(kT2Half)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -494,13 +661,25 @@ int tc2_max_pairs() {
 cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
     CUtensorMap mA, mB, mC;
     std::memset(&mC, 0, sizeof(mC));
-    if (!encode(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<void*>(a.A16), a.k, a.m, a.k_pitch * 2, kTcBK, kT2Half))
+    const bool widen = a.A8 != nullptr;
+    if (widen && (!a.int_out || (a.k % 16) != 0 || (reinterpret_cast<uintptr_t>(a.A8) % 16) != 0))
+        return cudaErrorInvalidValue;
+    if (widen ? !encode_a8(&mA, a.A8, a.k, a.m)
+              : !encode(&mA, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<void*>(a.A16), a.k, a.m, a.k_pitch * 2,
+                        kTcBK, kT2Half))
         return cudaErrorInvalidValue;
     if (!encode(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<void*>(a.B16), a.k, a.n, a.k_pitch * 2, kTcBK, kT2Half))
         return cudaErrorInvalidValue;
     const int64_t ldc = a.ldc > 0 ? a.ldc : a.n;
     if (ldc < a.n) return cudaErrorInvalidValue;
-    const bool c_tma = (ldc % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0;
+    // C may be absent only when every tile is requantised into rq.D
+    const bool requant = a.int_out && a.rq.qmode != kQuantNone;
+    if (a.C == nullptr && (!requant || (a.split_k > 1 && a.split_from < (a.m + 255) / 256 * ((a.n + 255) / 256))))
+        return cudaErrorInvalidValue;
+    if (requant && (a.rq.D == nullptr || a.rq.row_scale == nullptr || a.rq.col_scale == nullptr))
+        return cudaErrorInvalidValue;
+    // (no C at all: requantised output without split tiles)
+    const bool c_tma = a.C != nullptr && (ldc % 4) == 0 && (reinterpret_cast<uintptr_t>(a.C) % 16) == 0;
     if (c_tma && !encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.C, a.n, a.m, ldc * 4, 32, 32))
         return cudaErrorInvalidValue;
     T2Params p;
@@ -520,10 +699,13 @@ cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
     p.split_k = split ? a.split_k : 1;
     p.split_from = split ? static_cast<int>(a.split_from) : p.tiles;
     p.units = p.split_from + (p.tiles - p.split_from) * p.split_k;
+    p.rq = requant ? a.rq : RqOut{};
     const int pairs = tc2_pairs_for(a.grid, max_pairs, p.units);
-    const void* kern = a.int_out ? (c_tma ? tc2_kernel_ptr<true, true>() : tc2_kernel_ptr<true, false>())
-                                 : (c_tma ? tc2_kernel_ptr<false, true>() : tc2_kernel_ptr<false, false>());
-    cudaError_t e = configure2(kern);
+    const void* kern = widen ? (c_tma ? tc2_kernel_ptr<true, true, true>() : tc2_kernel_ptr<true, false, true>())
+                       : a.int_out ? (c_tma ? tc2_kernel_ptr<true, true>() : tc2_kernel_ptr<true, false>())
+                                   : (c_tma ? tc2_kernel_ptr<false, true>() : tc2_kernel_ptr<false, false>());
+    const size_t smem = widen ? kT2WSmem : kT2Smem;
+    cudaError_t e = configure2(kern, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
@@ -538,7 +720,7 @@ cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
-    cfg.dynamicSmemBytes = kT2Smem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 2;

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/dense_int8_matrix.h"
+
 namespace gemm {
 
 // ---- the tensor-core kernel family (gemm_tc.cu) ---------------------------
@@ -97,8 +99,33 @@ __host__ __device__ inline void tc_tile_coords(int t, int tiles_m, int tiles_n, 
     tn = local / rows_in_band;
 }
 
+// Requantised output (gemm_i8_run_requant): D[i][j] = q((float(C[i][j]) *
+// row_scale[i]) * col_scale[j]), q = bfloat16 or saturated int8 (requant.cuh).
+enum { kQuantNone = 0, kQuantBf16 = 1, kQuantI8 = 2 };
+struct RqOut {
+    void* D = nullptr;                  // m x n bfloat16 (bit patterns) or int8
+    const float* row_scale = nullptr;   // m floats, 16-byte aligned
+    const float* col_scale = nullptr;   // n floats, 16-byte aligned
+    int64_t ldd = 0;                    // row pitch of D in elements
+    int qmode = kQuantNone;             // kQuant*
+    int d_vec = 0;                      // 1: eight consecutive elements of a row take one 16-byte (bf16) / 8-byte (int8) store
+};
+// Tiles of a bm x bn tiling of C, [tile_from, tile_to) in tc_tile_coords
+// order; bm == 0: all of C.
+struct RqTiles {
+    int bm = 0, bn = 0;
+    int tiles_m = 0, tiles_n = 0;
+    int tile_from = 0, tile_to = 0;
+};
+// The elementwise requant kernel (requant.cu): D over the tiles `t` from the
+// int32 C (row pitch ldc), launched with programmatic stream serialization.
+cudaError_t launch_requant(const int32_t* C, int64_t ldc, const RqOut& o, int64_t m, int64_t n, const RqTiles& t,
+                           int num_sms, cudaStream_t stream);
+
 struct TcLaunch {
     const void* A16;      // m x k_pitch 16-bit operand (f16 for int8 problems, bf16 otherwise)
+    const void* A8 = nullptr;   // two-SM kernel, int8 problems: int8 A (m x k, k % 16 == 0) widened on chip
+                                // instead of A16
     const void* B16;      // n x k_pitch 16-bit operand
     void* C;              // m x n int32 (int8 problems) or fp32
     int* err;             // device error word
@@ -110,6 +137,10 @@ struct TcLaunch {
     int split_k;          // K slices of the tail tiles (1 = none); C must be zero over those tiles
     int64_t split_from;   // first split tile
     int64_t ldc = 0;      // row pitch of C in elements (0: n)
+    // int8 problems: whole tiles requantised into rq.D in the epilogue (split
+    // tiles still add their int32 partial sums into C, which may then be
+    // scratch); rq.qmode == kQuantNone: C as usual
+    RqOut rq;
 };
 
 cudaError_t launch_tc(const TcLaunch& a, cudaStream_t stream);
@@ -208,7 +239,11 @@ cudaError_t launch_skinny_tc(const int8_t* Bt, const uint16_t* A16, int32_t* C, 
 cudaError_t launch_skinny_i8(const int8_t* A, const int8_t* Bt, int32_t* C, int64_t m, int64_t n, int64_t k,
                              int num_sms, cudaStream_t stream);
 
-// ---- failure-detection self-test (selftest.cu) ------------------------------
+// ---- device error word and failure-detection self-test (selftest.cu) --------
+// Device address of the current device's error word (a static __device__ int
+// that every entry point's kernels write on a time-out and gemm_device_error
+// reads); call with the device current and cache per device.
+cudaError_t device_error_word(int** out);
 // One CTA waits on an mbarrier that nothing completes; the bounded wait gives
 // up after timeout_ns and records kDevErrTimeoutSelfTest in *err.
 cudaError_t launch_selftest_wait(int* err, uint64_t timeout_ns, cudaStream_t stream);
@@ -216,6 +251,13 @@ cudaError_t launch_selftest_wait(int* err, uint64_t timeout_ns, cudaStream_t str
 // ---- driver entry point for tensor-map encoding (gemm_tc.cu) ----------------
 bool tensor_map_encoder_available();
 void* tensor_map_encoder();   // cuTensorMapEncodeTiled, or nullptr
+
+// ---- argument checks shared by the entry points (api.cpp) -------------------
+// A plan from gemm_*_plan (or edited to another compiled tile / grid) for
+// `dtype`; GEMM_ERR_INVALID_ARG otherwise.
+gemm_status check_plan(const gemm_plan* plan, int32_t dtype);
+// Non-null device pointers, A and Bt 16-byte aligned, C 4-byte aligned.
+gemm_status check_ptrs(const void* A, const void* Bt, const void* C);
 
 // ---- kernel attributes (api.cpp) ---------------------------------------------
 // Opts `kern` in to `smem_bytes` of dynamic shared memory (and, if asked, the

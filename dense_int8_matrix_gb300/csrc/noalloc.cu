@@ -19,10 +19,13 @@
 // All calls share the one array and it keeps the last call's contents.  The
 // staging kernel (or, on the skinny path, the prologue that writes the f16
 // copy of A) overwrites every element the GEMM reads (the pad columns of each
-// row are never read), and the variant's time-out word is cleared at the
-// start of each call.  Calls whose work overlaps on the GPU (on different
+// row are never read).  Calls whose work overlaps on the GPU (on different
 // streams, or on different host threads without ordering) race on the array
 // and give wrong results: order them.
+//
+// A kernel wait that runs past its limit records its code in the device error
+// word that every entry point shares (itself a static __device__ variable, so
+// no allocation either); gemm_device_error reads and clears it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -38,9 +41,11 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // GEMM_NOALLOC_SCRATCH_BYTES
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-// Time-out word of this variant's kernels (the allocating entry points use
-// their own word, read by gemm_device_error).
-static __device__ int g_noalloc_err;
+
+// The skinny path's f16 copy of A (m <= 128 rows, k <= GEMM_I8_MAX_K) always
+// fits the array.
+static_assert(int64_t(128) * GEMM_I8_MAX_K * 2 <= int64_t(kNoAllocScratchBytes),
+              "skinny f16 activations must fit the static scratch");
 
 constexpr int kMaxDevices = 64;
 
@@ -50,7 +55,7 @@ struct NoAllocDevice {
     int num_sms = 0;
     int tc2_pairs = 0;                  // co-resident pairs of the two-SM kernel
     unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch
-    int* err = nullptr;                 // device address of g_noalloc_err
+    int* err = nullptr;                 // device address of the shared error word
 };
 
 std::mutex g_noalloc_mu;
@@ -75,9 +80,7 @@ gemm_status noalloc_device(NoAllocDevice** out) {
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
             d.scratch = static_cast<unsigned char*>(p);
-            p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_noalloc_err) != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
-            d.err = static_cast<int*>(p);
+            if (device_error_word(&d.err) != cudaSuccess) return GEMM_ERR_CUDA;
             d.tc2_pairs = tc2_max_pairs();
         }
         d.ready = true;
@@ -95,27 +98,23 @@ int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
 extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, const int8_t* Bt, int32_t* C,
                                            void* stream_ptr) {
     using namespace gemm;
-    if (!p || p->version != GEMM_PLAN_VERSION || p->dtype != GEMM_DTYPE_I8) return GEMM_ERR_INVALID_ARG;
-    if (p->m < 1 || p->k < 1 || p->n < 1) return GEMM_ERR_INVALID_ARG;
-    if (!A || !Bt || !C) return GEMM_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bt)) % 16 != 0 ||
-        reinterpret_cast<uintptr_t>(C) % 4 != 0)
-        return GEMM_ERR_MISALIGNED;
+    // the same plan and pointer checks as gemm_i8_run, then the scratch limit
+    gemm_status st = check_plan(p, GEMM_DTYPE_I8);
+    if (st != GEMM_OK) return st;
+    st = check_ptrs(A, Bt, C);
+    if (st != GEMM_OK) return st;
     const bool skinny = p->path == GEMM_PATH_SKINNY;
     if (skinny) {
-        if (p->m > 128 || p->k > GEMM_I8_MAX_K) return GEMM_ERR_INVALID_ARG;
-    } else {
-        const bool pair_tile = p->bm == 256 && p->bn == 256 && (p->grid % 2) == 0;
-        if (p->path != GEMM_PATH_TENSOR || (!pair_tile && p->bm != 64 && p->bm != 128) ||
-            (p->bn != 32 && p->bn != 64 && p->bn != 128 && p->bn != 256) || p->grid < 1 || p->k_pitch < p->k ||
-            (p->k_pitch % 8) != 0 || p->chunk_k < kTcBK || (p->chunk_k % kTcBK) != 0 || p->chunk_k > kI8ChunkK)
+        // f16 copy of A on the tensor-core skinny kernel (m * k * 2 bytes)
+        if (p->k > GEMM_I8_MAX_K || p->m * p->k * 2 > static_cast<int64_t>(kNoAllocScratchBytes))
             return GEMM_ERR_INVALID_ARG;
+    } else {
         // the f16 copies of A and Bt must fit the static scratch array
         const int64_t need = round256(p->m * p->k_pitch * 2) + round256(p->n * p->k_pitch * 2);
         if (need > static_cast<int64_t>(kNoAllocScratchBytes)) return GEMM_ERR_INVALID_ARG;
     }
     NoAllocDevice* d = nullptr;
-    gemm_status st = noalloc_device(&d);
+    st = noalloc_device(&d);
     if (st != GEMM_OK) return st;
     if (!d->supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -124,7 +123,6 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
         if (skinny_tc_supported(p->m, p->n, p->k, A, Bt) && tensor_map_encoder_available()) {
             // as in gemm_i8_run, with the f16 copy of A (m * k * 2 <= 32 MiB for
             // any k the planner accepts) at the start of the static array
-            if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;
             uint16_t* A16 = reinterpret_cast<uint16_t*>(d->scratch);
             if (launch_skinny_prologue(A, A16, C, p->m, p->n, p->k, d->num_sms, stream) != cudaSuccess ||
                 launch_skinny_tc(Bt, A16, C, d->err, p->m, p->n, p->k, d->num_sms, stream) != cudaSuccess)
@@ -136,7 +134,6 @@ extern "C" gemm_status gemm_i8_run_noalloc(const gemm_plan* p, const int8_t* A, 
     }
 
     if (!tensor_map_encoder_available()) return GEMM_ERR_CUDA;
-    if (cudaMemsetAsync(d->err, 0, sizeof(int), stream) != cudaSuccess) return GEMM_ERR_CUDA;
     uint16_t* Ah = reinterpret_cast<uint16_t*>(d->scratch);
     uint16_t* Bh = reinterpret_cast<uint16_t*>(d->scratch + round256(p->m * p->k_pitch * 2));
     // K split as in gemm_i8_run: the staging kernel zeroes C over the split tiles

@@ -20,6 +20,9 @@
 //   (unstated tie-break)      larger BM*BN, then larger BM
 //   claim 7                   every tile is a compiled template instance; the
 //                             plan names the one to launch
+//   (after step 5)            a multi-wave choice gives way to the two-SM
+//                             tile when it covers C in one round of pairs and
+//                             K has at least 12 steps
 //   (after step 5, int8)      K split: small-MN, large-K problems whose choice
 //                             runs in one wave take the two-SM tile split
 //                             along K; otherwise the tail of a partial last
@@ -40,6 +43,12 @@ constexpr int64_t kSmemPerSm = 233472;
 constexpr int64_t kRegsPerSm = 65536;
 constexpr int64_t kTmemColsPerSm = 512;
 constexpr int64_t kMaxDim = 2147483647;
+// Widen int8 A on chip in the two-SM kernel when C is at most this wide: the
+// staged f16 copy of A costs 3 m*k bytes of traffic against 2 m*n*k flops.
+constexpr int64_t kAOnChipMaxN = 256;
+// The two-SM tile replaces a multi-wave one-SM choice only with at least this
+// many K steps of 64.
+constexpr int64_t kPairWaveMinKSteps = 12;
 
 struct Tile {
     int bm, bn;
@@ -80,6 +89,14 @@ int tile_bpc(const Tile& t) {
 }
 
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// After the tile and the K split: int8 problems on the two-SM tile with a
+// narrow C and a 16-byte row pitch of int8 A widen A on chip; the workspace
+// then holds only the f16 copy of Bt.
+void set_a_on_chip(gemm_plan* p) {
+    p->a_on_chip = (p->dtype == GEMM_DTYPE_I8 && p->bm == 256 && p->k % 16 == 0 && p->n <= kAOnChipMaxN) ? 1 : 0;
+    if (p->a_on_chip) p->workspace_bytes = round_up(p->n * p->k_pitch * 2, 256);
+}
 
 }  // namespace
 
@@ -182,6 +199,24 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
         }
     }
     if (best < 0) return GEMM_ERR_INVALID_ARG;
+
+    // Beyond the five steps (measured): a choice of two or more waves gives
+    // way to the two-SM tile in one wave when that tile covers C in one round
+    // of CTA pairs (step 3 rejected it for filling fewer than all SMs) and K
+    // has at least kPairWaveMinKSteps steps.  Each SM then does the same
+    // multiply-adds as in two waves of one-SM tiles, from half the staged
+    // bytes per flop; with shorter K the two-SM tile's pipeline fill and
+    // epilogue, which no second wave hides, cost more than that saves.
+    {
+        const int pair_idx = kNumTiles - 1;   // {256, 256}
+        const Tile& pt = kTiles[pair_idx];
+        const int64_t t2 = out_tiles(pt, m, n);
+        if (best_waves >= 2 && !is_pair(kTiles[best]) && tile_fits(pt) && t2 <= num_sms / 2 &&
+            ceil_div(k, kTcBK) >= kPairWaveMinKSteps) {
+            best = pair_idx;
+            best_waves = ceil_div(out_ctas(pt, m, n), static_cast<int64_t>(num_sms) * tile_bpc(pt));
+        }
+    }
     const Tile& t = kTiles[best];
     const int64_t tiles = out_tiles(t, m, n);
     if (tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
@@ -239,6 +274,7 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
             p.ratio = tile_ratio(pair_tile);
             p.split_k = static_cast<int32_t>(s);
             p.split_from = 0;
+            set_a_on_chip(&p);
             *out = p;
             return GEMM_OK;
         }
@@ -250,6 +286,7 @@ gemm_status make_plan(int32_t dtype, int64_t m, int64_t k, int64_t n, int32_t nu
     const int64_t workers = is_pair(t) ? p.grid / 2 : p.grid;
     p.split_k = tc_tail_split(tiles, workers, nchunks, dtype == GEMM_DTYPE_I8, &split_from);
     p.split_from = static_cast<int32_t>(split_from);
+    set_a_on_chip(&p);
     *out = p;
     return GEMM_OK;
 }

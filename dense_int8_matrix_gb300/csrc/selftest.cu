@@ -1,6 +1,16 @@
-// Failure-detection self-test: proves on the device that a bounded wait on a
-// barrier that never completes gives up, records an error code the host can
-// read, and leaves the context usable.  Nothing faults, traps or hangs.
+// The device error word and the failure-detection self-test.
+//
+// Every bounded wait in the library's kernels that gives up records its code
+// in one int per device (first code wins; kernels only write it).  The word is
+// a file-scope static __device__ variable, so no entry point allocates it and
+// the allocating and allocation-free entry points share it; gemm_device_error
+// reads and clears it.  In host code the variable's name is a host-side
+// stand-in, so device_error_word() looks its device address up with
+// cudaGetSymbolAddress (callers cache it per device).
+//
+// The self-test proves on the device that a bounded wait on a barrier that
+// never completes gives up, records an error code the host can read, and
+// leaves the context usable.  Nothing faults, traps or hangs.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -9,6 +19,8 @@
 namespace gemm {
 
 namespace {
+
+static __device__ int g_device_err;
 
 __global__ void selftest_wait_kernel(int* err, uint64_t timeout_ns) {
     __shared__ __align__(8) uint64_t bar;
@@ -25,6 +37,15 @@ __global__ void selftest_wait_kernel(int* err, uint64_t timeout_ns) {
 }
 
 }  // namespace
+
+cudaError_t device_error_word(int** out) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_device_err);
+    if (e != cudaSuccess) return e;
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    *out = static_cast<int*>(p);
+    return cudaSuccess;
+}
 
 cudaError_t launch_selftest_wait(int* err, uint64_t timeout_ns, cudaStream_t stream) {
     selftest_wait_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);

@@ -85,6 +85,19 @@ def random_bf16(shape, seed: int, scale: float = 1.0) -> torch.Tensor:
     return (x * scale).to(torch.bfloat16)
 
 
+def requant_scales(m: int, n: int, k: int, seed: int, c_std_per_sqrt_k: float = 5461.0, target: float = 40.0):
+    """Seeded per-row and per-column fp32 scales for requantising an int32
+    product of depth k: each drawn uniformly from [0.5, 1.5) times a base, so
+    that their product times the typical |C| (c_std_per_sqrt_k * sqrt(k);
+    5461 for int8 uniform in [-128, 127]) is about `target` (some int8
+    results saturate, bfloat16 results span several binades)."""
+    g = generator(seed)
+    base = (target / (c_std_per_sqrt_k * float(k) ** 0.5)) ** 0.5
+    rs = (torch.rand((m,), generator=g, dtype=torch.float32) + 0.5) * base
+    cs = (torch.rand((n,), generator=g, dtype=torch.float32) + 0.5) * base
+    return rs, cs
+
+
 def shape_seed(tag: str) -> int:
     """A stable seed derived from a text tag (for test cases)."""
     return int.from_bytes(hashlib.sha256(tag.encode()).digest()[:4], "little")

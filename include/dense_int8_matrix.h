@@ -70,8 +70,12 @@ enum {
     GEMM_KERNEL_STAGE = 0,  /* operand staging: int8 -> f16 widening / re-pitching */
     GEMM_KERNEL_TC = 1,     /* tcgen05 tensor-core GEMM */
     GEMM_KERNEL_SKINNY = 2, /* skinny-m GEMM */
-    GEMM_KERNEL_KINDS = 3
+    GEMM_KERNEL_REQUANT = 3, /* elementwise requantisation (gemm_i8_run_requant: K-split tiles, skinny path) */
+    GEMM_KERNEL_KINDS = 4
 };
+
+/* Output types of gemm_i8_run_requant. */
+enum { GEMM_OUT_BF16 = 1, GEMM_OUT_I8 = 2 };
 
 #define GEMM_PLAN_VERSION 2
 #define GEMM_I8_MAX_K 131071 /* 131071 * 128 * 128 < 2^31 */
@@ -109,7 +113,8 @@ typedef struct gemm_plan {
     double ratio;        /* compute-to-memory ratio of the tile (claim 5), flop per byte */
     int64_t workspace_bytes; /* device scratch gemm_*_run takes from its pool (16-bit operand copies) */
     int32_t split_from;  /* tiles [split_from, tiles) are split into split_k K slices */
-    int32_t reserved0;
+    int32_t a_on_chip;   /* 1: the two-SM kernel loads int8 A and widens it on chip (no f16 copy of A);
+                            int8, bm == 256 and k % 16 == 0 only (see gemm_i8_plan) */
     int64_t reserved[3];
 } gemm_plan;
 
@@ -117,7 +122,10 @@ typedef struct gemm_plan {
  * Plan an int8 problem (m x k) x (k x n) for the current CUDA device.
  * Routing: m <= 64, or m <= 128 with k % 16 == 0 -> skinny path (streams Bt
  * once, widening it on chip); otherwise the five
- * steps of CN114238853A claim 1 select a (BM, BN) tile.  Host-only apart from
+ * steps of CN114238853A claim 1 select a (BM, BN) tile.  When the two-SM tile
+ * runs a narrow C (n <= 256) with k % 16 == 0, a_on_chip = 1: A is widened
+ * from int8 inside the GEMM instead of through a staged f16 copy, which for
+ * such shapes would move more bytes than the multiply.  Host-only apart from
  * one cached query of the device's SM count.
  * Errors: GEMM_ERR_INVALID_ARG (out == NULL, m/k/n outside [1, 2^31-1]),
  * GEMM_ERR_OVERFLOW_RISK (k > GEMM_I8_MAX_K), GEMM_ERR_CUDA (no device).
@@ -160,6 +168,33 @@ GEMM_API gemm_status gemm_bf16_run(const gemm_plan *plan, const uint16_t *A, con
                           void *stream);
 
 /*
+ * Requantising int8 GEMM: D = q( (float(C[i][j]) * row_scale[i]) * col_scale[j] )
+ * for the exact int32 product C = A x B of gemm_i8_run, the usual consumer of
+ * an int8 GEMM (per-row activation scales, per-column weight scales, a
+ * narrower output).  The pages do not define requantisation; its arithmetic is
+ * the library's and is stated here: every step is one IEEE-754 binary32
+ * operation rounded to nearest, ties to even - (1) int32 -> float, (2) times
+ * the row scale, (3) times the column scale - then q:
+ *   GEMM_OUT_BF16  bfloat16, round to nearest even (overflow gives infinity,
+ *                  NaN stays NaN); D holds m x n 16-bit patterns;
+ *   GEMM_OUT_I8    int8: nearest integer, ties to even, then clamped to
+ *                  [-128, 127]; NaN gives 0; D holds m x n int8.
+ * Where one CTA completes a tile of C, the tile is requantised in the GEMM's
+ * epilogue and C never reaches memory (the shared-memory staged write-back of
+ * "先导杯比赛回顾", section "Epilogue 写回优化", carried one step further).  The
+ * tiles of a K split and the skinny path's C are completed in int32 scratch
+ * from the library's pool and converted by a second, elementwise kernel.
+ * Same plan and operand rules as gemm_i8_run.  row_scale (m floats) and
+ * col_scale (n floats) are device pointers, 16-byte aligned; D is a device
+ * pointer (2-byte aligned for bfloat16), row pitch n.
+ * Errors: GEMM_ERR_INVALID_ARG (null pointer, bad plan or out_type),
+ * GEMM_ERR_MISALIGNED, GEMM_ERR_UNSUPPORTED_DEVICE, GEMM_ERR_CUDA.
+ */
+GEMM_API gemm_status gemm_i8_run_requant(const gemm_plan *plan, const int8_t *A, const int8_t *Bt,
+                                         const float *row_scale, const float *col_scale, int32_t out_type, void *D,
+                                         void *stream);
+
+/*
  * gemm_i8_run without any device-memory allocation.  The pages have no
  * counterpart to this entry point.
  *
@@ -184,9 +219,10 @@ GEMM_API gemm_status gemm_bf16_run(const gemm_plan *plan, const uint16_t *A, con
  *     (each call overwrites what it reads and clears its own time-out word),
  *     so calls whose work overlaps on the GPU race and give wrong results:
  *     order them on one stream or with events;
- *   - a kernel wait that runs past its limit ends this variant's kernels
- *     early (C incomplete) and is recorded in the variant's own device word,
- *     which gemm_device_error does not read.
+ *   - a kernel wait that runs past its limit ends the call's kernels early
+ *     (C incomplete) and records its code in the device error word that all
+ *     entry points share (a static device variable, not an allocation):
+ *     gemm_device_error reports it as for gemm_i8_run.
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES (64ll << 20)
 GEMM_API gemm_status gemm_i8_run_noalloc(const gemm_plan *plan, const int8_t *A, const int8_t *Bt, int32_t *C,
@@ -212,12 +248,27 @@ GEMM_API gemm_status gemm_bf16_run_host(const gemm_plan *plan, const uint16_t *A
                                void *stream);
 
 /*
- * Waits for `stream`, then reads and clears the current device's error word.
+ * Waits for `stream`, then reads and clears the current device's error word,
+ * which the kernels of every run entry point (gemm_i8_run_noalloc included)
+ * write when a wait gives up; the first code since the last read is kept.
  * Returns GEMM_OK, GEMM_ERR_TIMEOUT (a kernel wait ran past its 2 s limit
  * and the kernel returned early; *code gets the stage that gave up) or
  * GEMM_ERR_CUDA.  `code` may be NULL.
  */
 GEMM_API gemm_status gemm_device_error(void *stream, int32_t *code);
+
+/*
+ * The library's private stream-ordered memory pool on the current device
+ * (the scratch of gemm_*_run and the device buffers of gemm_*_run_host):
+ * bytes it holds now (*reserved_bytes) and the most bytes in use at once
+ * since the pool was created or the mark was last reset (*used_high_bytes).
+ * reset_high != 0 restarts that mark from the current use after reading it.
+ * For callers that budget device memory; the pool keeps freed memory for the
+ * next call and returns it only when the process exits.
+ * Errors: GEMM_ERR_INVALID_ARG (NULL output), GEMM_ERR_UNSUPPORTED_DEVICE,
+ * GEMM_ERR_CUDA.
+ */
+GEMM_API gemm_status gemm_pool_usage(int64_t *reserved_bytes, int64_t *used_high_bytes, int32_t reset_high);
 
 /*
  * Tracing.  While enabled, every kernel launch made by gemm_*_run is counted

@@ -13,10 +13,13 @@ first can be checked against the patent alone:
    given, and the library's compiled kernels are one such table
    (``library_candidates``).
 2. The library's own rules, which the pages do not contain: ``route`` sends
-   small-m int8 problems to the skinny path before step 1, and ``k_split``
-   splits small-MN, large-K int8 problems along K after step 5.
+   small-m int8 problems to the skinny path before step 1; after step 5,
+   ``pair_wave`` trades a multi-wave choice for the two-SM tile in one wave,
+   ``k_split`` splits small-MN, large-K int8 problems along K, and
+   ``a_on_chip`` says where int8 A is widened to f16.
 
-``select`` composes them: route, then the five steps, then the K split.
+``select`` composes them: route, the five steps, pair_wave, the K split,
+a_on_chip.
 
 Readings of the five steps (the patent's formulas did not survive
 extraction):
@@ -179,6 +182,27 @@ def route(dtype: str, m: int, k: int) -> str:
     return "tensor"
 
 
+PAIR_WAVE_MIN_K_STEPS = 12
+
+
+def pair_wave(m: int, k: int, n: int, num_sms: int, chosen: dict) -> dict:
+    """After step 5: when the five steps' choice needs two or more waves,
+    while the two-SM tile (which step 3 rejects for filling fewer than all
+    SMs) covers C in one round of CTA pairs (T2 = ceil(m/256) * ceil(n/256)
+    <= floor(SMs / 2)) and K has at least 12 steps of 64 (ceil(k/64) >= 12),
+    the two-SM tile replaces it: one wave, T2 tiles.  Each SM then does the
+    same multiply-adds as in the two waves of one-SM tiles, from half the
+    staged bytes per flop."""
+    if chosen["waves"] < 2 or chosen["bm"] == 256:
+        return chosen
+    t2 = tiles(m, n, 256, 256)
+    if t2 > num_sms // 2 or math.ceil(k / BK_ELEMS) < PAIR_WAVE_MIN_K_STEPS:
+        return chosen
+    pair = candidate(256, 256)
+    return {"bm": 256, "bn": 256, "tiles": t2, "bpc": blocks_per_sm(pair),
+            "waves": waves(m, n, pair, num_sms), "fallback": chosen["fallback"]}
+
+
 def k_split(dtype: str, m: int, k: int, n: int, num_sms: int, chosen: dict) -> dict:
     """After step 5, int8 only (the slices of an int8 product add exactly):
     when the five steps' choice runs in one wave, the two-SM tile split into
@@ -202,13 +226,23 @@ def k_split(dtype: str, m: int, k: int, n: int, num_sms: int, chosen: dict) -> d
             "fallback": chosen["fallback"], "split": s}
 
 
+A_ON_CHIP_MAX_N = 256
+
+
+def a_on_chip(dtype: str, k: int, n: int, chosen: dict) -> int:
+    """After the K split: int8 problems on the two-SM tile with n <= 256 and k
+    a multiple of 16 widen int8 A inside the GEMM instead of staging an f16
+    copy (for a narrow C that copy moves more bytes than the multiply)."""
+    return int(dtype == "i8" and chosen["bm"] == 256 and k % 16 == 0 and n <= A_ON_CHIP_MAX_N)
+
+
 def select(dtype: str, m: int, k: int, n: int, num_sms: int) -> dict:
     """The whole selection the library's planner makes: route, the five
-    steps, the K split."""
+    steps, the pair-tile wave rule, the K split, where A is widened."""
     if route(dtype, m, k) == "skinny":
         return {"path": "skinny"}
-    chosen = five_steps(m, n, num_sms)
-    return dict(k_split(dtype, m, k, n, num_sms, chosen), path="tensor")
+    chosen = k_split(dtype, m, k, n, num_sms, pair_wave(m, k, n, num_sms, five_steps(m, n, num_sms)))
+    return dict(chosen, path="tensor", a_on_chip=a_on_chip(dtype, k, n, chosen))
 
 
 # Kept for the tests that look a candidate up by its tile.

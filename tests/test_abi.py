@@ -61,13 +61,17 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_plan_struct_layout(lib):
-    p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 1000, 777, 3000, 148)
+    # k = 700: 11 K steps, so the five steps' (128, 128) choice stands
+    p = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 1000, 700, 3000, 148)
     assert ctypes.sizeof(B.gemm_plan) == 136
-    assert (p.version, p.m, p.k, p.n) == (B.GEMM_PLAN_VERSION, 1000, 777, 3000)
-    assert (p.bm, p.bn, p.tiles, p.waves) == (128, 128, 192, 2)
-    assert p.k_pitch == 784 and p.chunk_k == 1024 and p.bk == 64 and p.stages == 4
-    assert p.workspace_bytes == (1000 * 784 * 2 + 255) // 256 * 256 + (3000 * 784 * 2 + 255) // 256 * 256
+    assert (p.version, p.m, p.k, p.n) == (B.GEMM_PLAN_VERSION, 1000, 700, 3000)
+    assert (p.bm, p.bn, p.tiles, p.waves, p.a_on_chip) == (128, 128, 192, 2, 0)
+    assert p.k_pitch == 704 and p.chunk_k == 1024 and p.bk == 64 and p.stages == 4
+    assert p.workspace_bytes == (1000 * 704 * 2 + 255) // 256 * 256 + (3000 * 704 * 2 + 255) // 256 * 256
     assert abs(p.ratio - 64.0) < 1e-12
+    # the narrow shape widens A on chip: only the f16 copy of Bt is staged
+    q = B.gemm_plan_for_sms(B.GEMM_DTYPE_I8, 4097, 16384, 255, 148)
+    assert (q.bm, q.a_on_chip, q.workspace_bytes) == (256, 1, 255 * 16384 * 2)
 
 
 @pytest.mark.parametrize("ex", EXAMPLES, ids=lambda e: "%s-%dx%dx%d-%d" % e[:5])
@@ -100,9 +104,9 @@ def test_planner_matches_selector_oracle_sweep(lib):
         if want["path"] == "skinny":
             assert p.path == B.GEMM_PATH_SKINNY
             continue
-        got = (p.bm, p.bn, p.tiles, p.waves, p.bpc, bool(p.fallback))
+        got = (p.bm, p.bn, p.tiles, p.waves, p.bpc, bool(p.fallback), p.a_on_chip)
         assert got == (want["bm"], want["bn"], want["tiles"], want["waves"], want["bpc"],
-                       want["fallback"]), (d, m, k, n, sms)
+                       want["fallback"], want["a_on_chip"]), (d, m, k, n, sms)
         if want["split"] > 1:   # every tile split: all slices in one round of pairs
             assert (p.split_k, p.split_from) == (want["split"], 0)
             assert p.grid == 2 * p.tiles * p.split_k <= 2 * (sms // 2)

@@ -74,11 +74,26 @@ def test_library_selection_hand_examples(ex):
 
 def test_five_steps_do_not_depend_on_k_or_dtype():
     # the patent's steps see only the output tiling: k and the dtype enter
-    # through the library's routing and K split alone
-    for m, n in [(1000, 3000), (4097, 255), (8192, 8192)]:
-        a = selector.select("bf16", m, 4096, n, 148)
-        b = selector.five_steps(m, n, 148)
-        assert (a["bm"], a["bn"], a["tiles"], a["waves"]) == (b["bm"], b["bn"], b["tiles"], b["waves"])
+    # through the library's rules alone, none of which applies with 8 K steps
+    for m, n in [(1000, 3000), (4097, 255), (8192, 8192), (2048, 2048)]:
+        for d in ("bf16", "i8"):
+            a = selector.select(d, m, 512, n, 148)
+            b = selector.five_steps(m, n, 148)
+            assert (a["bm"], a["bn"], a["tiles"], a["waves"]) == (b["bm"], b["bn"], b["tiles"], b["waves"])
+
+
+def test_pair_wave_rule():
+    # a multi-wave one-SM choice gives way to the two-SM tile in one wave only
+    # when T2 fits one round of pairs and K has at least 12 steps
+    assert selector.select("i8", 1000, 777, 3000, 148)["bm"] == 256
+    assert selector.select("i8", 1000, 704, 3000, 148)["bm"] == 128      # 11 K steps
+    # step 3 rejects the two-SM tile exactly when its CTAs (2 T2) are fewer
+    # than the SMs, i.e. when it fits one round of pairs; a larger problem
+    # keeps the five steps' own two-SM choice, in two waves
+    got = selector.select("i8", 2500, 4096, 3000, 148)
+    assert (got["bm"], got["tiles"], got["waves"]) == (256, 120, 2)
+    got = selector.select("bf16", 3000, 1000, 1000, 152)
+    assert (got["bm"], got["tiles"], got["waves"]) == (256, 48, 1)
 
 
 def test_ratio_closed_form():
