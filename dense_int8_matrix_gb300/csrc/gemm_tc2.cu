@@ -61,10 +61,12 @@ constexpr int kT2EpiBytes = kTcEpilogueWarps * kTcEpiStageBytes;
 constexpr size_t kT2Smem = static_cast<size_t>(kT2Stages) * kT2StageBytes + kT2EpiBytes + 1024 + 1024;
 static_assert(kT2Smem == tc2_smem_bytes(), "shared-memory size known to the planner");
 
-// Widened-A variant: a 5-stage f16 operand ring and a 4-stage ring of int8 A
-// (128 rows x 64 bytes = 8 KiB per stage and CTA).
-constexpr int kT2WStages = 5;
-constexpr int kT2W8Stages = 4;
+// Widened-A variant: a 4-stage f16 operand ring (filled by TMA for Bt and by
+// the widening warps for A, on chip, so it needs little depth) and an 8-stage
+// ring of int8 A (128 rows x 64 bytes = 8 KiB per stage and CTA) that covers
+// the latency of the int8 stream from HBM.
+constexpr int kT2WStages = 4;
+constexpr int kT2W8Stages = 8;
 constexpr int kT2W8Bytes = kT2Half * kTcBK;        // 8 KiB
 constexpr int kT2WidenThreads = 64;                // warps 2 and 3
 constexpr size_t kT2WSmem = static_cast<size_t>(kT2WStages) * kT2StageBytes +
@@ -342,7 +344,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer --
-        if (lane == 0) {
+        if (WIDEN_A && lane == 1) {
+            // int8 A into its own ring, gated only by the widening group's
+            // releases (not by the f16 slots), so the HBM stream runs up to
+            // kT2W8Stages K steps ahead
+            pdl_wait();
+            const uint64_t pol = policy_evict_first();
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int u = pair; ok && u < p.units; u += npairs) {
+                const Unit2 w = unit_at2(u, p);
+                const int ya = w.tm * 256 + static_cast<int>(rank) * kT2Half;
+                for (int kb = w.kb_lo; kb < w.kb_hi; ++kb) {
+                    const uint32_t s8 = issued % kT2W8Stages, ph8 = (issued / kT2W8Stages) & 1u;
+                    if (!wait_bounded(a8empty_bar0 + 8u * s8, ph8 ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(a8full_bar0 + 8u * s8, kT2W8Bytes);
+                    tma_load_2d(sA8 + s8 * kT2W8Bytes, &tmA, kb * kTcBK, ya, a8full_bar0 + 8u * s8, pol);
+                    ++issued;
+                }
+            }
+            // Teardown: the copies still in flight must land before the CTA
+            // exits (earlier ones were waited for by the widening group
+            // before their slot was reused)
+            for (uint32_t j = issued > static_cast<uint32_t>(kT2W8Stages) ? issued - kT2W8Stages : 0u; j < issued;
+                 ++j)
+                wait_bounded(a8full_bar0 + 8u * (j % kT2W8Stages), (j / kT2W8Stages) & 1u, nullptr, p.err,
+                             kDevErrTimeoutTeardown);
+        } else if (lane == 0) {
             pdl_wait();   // the operands may come from the staging kernel just before
             const uint64_t pol = policy_evict_normal();
             uint32_t issued = 0;
@@ -360,16 +391,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     const uint32_t fb = map_to_rank(full_bar0 + 8u * s, 0);
                     if constexpr (WIDEN_A) {
-                        // int8 A into its own ring (local barrier); only the
-                        // bytes of Bt complete on the even CTA's barrier
-                        const uint32_t s8 = issued % kT2W8Stages, ph8 = (issued / kT2W8Stages) & 1u;
-                        if (!wait_bounded(a8empty_bar0 + 8u * s8, ph8 ^ 1u, abort_flag, p.err,
-                                          kDevErrTimeoutProducer)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(a8full_bar0 + 8u * s8, kT2W8Bytes);
-                        tma_load_2d(sA8 + s8 * kT2W8Bytes, &tmA, kb * kTcBK, ya, a8full_bar0 + 8u * s8, pol);
+                        // A comes from the widening warps (lane 1 streams the
+                        // int8 bytes); only the bytes of Bt complete on the
+                        // even CTA's barrier
                         if (leader) mbar_arrive_expect_tx(full_bar0 + 8u * s, 2 * kT2HalfBytes);
                     } else {
                         // both CTAs' copies complete on the even CTA's barrier,
@@ -380,15 +404,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_load_2d_pair(sB + s * kT2HalfBytes, &tmB, kb * kTcBK, yb, fb, pol);
                     ++issued;
                 }
-            }
-            if constexpr (WIDEN_A) {
-                // Teardown: the int8 copies still in flight must land before
-                // the CTA exits (earlier ones were waited for by the widening
-                // group before their slot was reused)
-                for (uint32_t j = issued > static_cast<uint32_t>(kT2W8Stages) ? issued - kT2W8Stages : 0u;
-                     j < issued; ++j)
-                    wait_bounded(a8full_bar0 + 8u * (j % kT2W8Stages), (j / kT2W8Stages) & 1u, nullptr, p.err,
-                                 kDevErrTimeoutTeardown);
             }
         }
     } else if (WIDEN_A && (warp == 2 || warp == 3)) {
