@@ -27,9 +27,9 @@
 // Widened A (int8 problems with k % 16 == 0, chosen by the caller for narrow
 // C, where a staged f16 copy of A would cost more traffic than the multiply):
 // int8 A is loaded by TMA (128 rows x 64 bytes per K step) into a separate
-// ring, and warps 2-3 of each CTA widen it exactly to f16 in the 128-byte
-// swizzled layout of the operand ring, so A crosses HBM once, as int8; Bt
-// still comes from the staged f16 copy.  The widened halves of both CTAs are
+// ring, and warps 2 and 3 of each CTA (alternate K steps) widen it exactly to
+// f16 in the 128-byte swizzled layout of the operand ring, so A crosses HBM
+// once, as int8; Bt still comes from the staged f16 copy.  The widened halves of both CTAs are
 // announced on the even CTA's "full" barrier beside the TMA bytes of Bt.
 //
 // Tail split (int8 problems): when the last round of pairs is only partly
@@ -68,7 +68,6 @@ static_assert(kT2Smem == tc2_smem_bytes(), "shared-memory size known to the plan
 constexpr int kT2WStages = 4;
 constexpr int kT2W8Stages = 8;
 constexpr int kT2W8Bytes = kT2Half * kTcBK;        // 8 KiB
-constexpr int kT2WidenThreads = 64;                // warps 2 and 3
 constexpr size_t kT2WSmem = static_cast<size_t>(kT2WStages) * kT2StageBytes +
                             static_cast<size_t>(kT2W8Stages) * kT2W8Bytes + kT2EpiBytes + 1024 + 1024;
 static_assert(kT2WSmem <= 232448, "widened-A shared memory");
@@ -171,21 +170,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
             bar),
         "h"(mask)
         : "memory");
-}
-
-// Named barrier 1 of the two widening warps (64 threads).
-__device__ __forceinline__ void widen_group_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
-// The same barrier, returning whether `pred` holds in every thread of the
-// group, so that both warps leave their loop together or not at all.
-__device__ __forceinline__ bool widen_group_all(int pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(pred)
-        : "memory");
-    return r != 0;
 }
 
 // Arrive on a barrier given by its shared::cluster address with the default
@@ -408,16 +392,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (WIDEN_A && (warp == 2 || warp == 3)) {
         // --------------------------------------------- widen int8 A to f16 --
-        // Per K step: 128 rows x 64 int8 (512 chunks of 16 bytes, eight per
-        // thread) -> 128 rows x 64 f16 in the 128-byte swizzled layout the
-        // MMA descriptor reads (chunk c of row r at ((c ^ (r & 7)) << 4)).
-        const int t = threadIdx.x - 64;   // 0..63
+        // Warps 2 and 3 take alternate K steps, each on its own: 128 rows x
+        // 64 int8 (512 chunks of 16 bytes, sixteen per lane) -> 128 rows x
+        // 64 f16 in the 128-byte swizzled layout the MMA descriptor reads
+        // (chunk c of row r at ((c ^ (r & 7)) << 4)).  With 8 int8 and 4 f16
+        // slots the two warps use disjoint slots, so every barrier has a
+        // single waiter sequence per warp.
+        const uint32_t g = static_cast<uint32_t>(warp - 2);
         uint32_t done = 0;
         bool ok = true;
         const uint32_t fb = map_to_rank(full_bar0, 0);
         for (int u = pair; ok && u < p.units; u += npairs) {
             const Unit2 w = unit_at2(u, p);
-            for (int kb = w.kb_lo; kb < w.kb_hi; ++kb) {
+            for (int kb = w.kb_lo; kb < w.kb_hi; ++kb, ++done) {
+                if ((done & 1u) != g) continue;
                 const uint32_t s = done % kStages, ph = (done / kStages) & 1u;
                 const uint32_t s8 = done % kT2W8Stages, ph8 = (done / kT2W8Stages) & 1u;
                 int got = 1;
@@ -427,21 +415,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                               ? 1
                               : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
-                if (!widen_group_all(got)) {   // both warps leave together
+                if (!got) {
                     ok = false;
                     break;
                 }
                 const uint32_t src = sA8 + s8 * kT2W8Bytes;
                 const uint32_t dst = sA + s * kT2HalfBytes;
-                // all eight loads first (the shared-memory accesses are
+                // all sixteen loads first (the shared-memory accesses are
                 // volatile asm, which the compiler keeps in program order),
                 // then widen and store
-                uint4 v[8];
+                uint4 v[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = ld_shared_v4(src + (t + kT2WidenThreads * i) * 16);
+                for (int i = 0; i < 16; ++i) v[i] = ld_shared_v4(src + (lane + 32 * i) * 16);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int q = t + kT2WidenThreads * i;   // 16-byte int8 chunk: row q / 4, chunk q % 4
+                for (int i = 0; i < 16; ++i) {
+                    const int q = lane + 32 * i;   // 16-byte int8 chunk: row q / 4, chunk q % 4
                     const int r = q >> 2, c = q & 3;
                     uint32_t wv[8];
                     widen16(v[i], wv);
@@ -450,12 +438,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     st_shared_v4(row + (((2 * c + 1) ^ (r & 7)) << 4), wv[4], wv[5], wv[6], wv[7]);
                 }
                 fence_proxy_async_smem();   // the MMA (async proxy) reads what was just written
-                widen_group_sync();
-                if (t == 0) {
+                __syncwarp();
+                if (lane == 0) {
                     mbar_arrive(a8empty_bar0 + 8u * s8);
                     mbar_arrive_remote(fb + 8u * s);
                 }
-                ++done;
             }
         }
     } else if (warp == 1) {

@@ -45,7 +45,7 @@ constexpr int64_t kTmemColsPerSm = 512;
 constexpr int64_t kMaxDim = 2147483647;
 // Widen int8 A on chip in the two-SM kernel when C is at most this wide: the
 // staged f16 copy of A costs 3 m*k bytes of traffic against 2 m*n*k flops.
-constexpr int64_t kAOnChipMaxN = 256;
+constexpr int64_t kAOnChipMaxN = 512;
 // The two-SM tile replaces a multi-wave one-SM choice only with at least this
 // many K steps of 64.
 constexpr int64_t kPairWaveMinKSteps = 12;

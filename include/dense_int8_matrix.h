@@ -123,7 +123,7 @@ typedef struct gemm_plan {
  * Routing: m <= 64, or m <= 128 with k % 16 == 0 -> skinny path (streams Bt
  * once, widening it on chip); otherwise the five
  * steps of CN114238853A claim 1 select a (BM, BN) tile.  When the two-SM tile
- * runs a narrow C (n <= 256) with k % 16 == 0, a_on_chip = 1: A is widened
+ * runs a narrow C (n <= 512) with k % 16 == 0, a_on_chip = 1: A is widened
  * from int8 inside the GEMM instead of through a staged f16 copy, which for
  * such shapes would move more bytes than the multiply.  Host-only apart from
  * one cached query of the device's SM count.

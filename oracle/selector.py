@@ -226,11 +226,11 @@ def k_split(dtype: str, m: int, k: int, n: int, num_sms: int, chosen: dict) -> d
             "fallback": chosen["fallback"], "split": s}
 
 
-A_ON_CHIP_MAX_N = 256
+A_ON_CHIP_MAX_N = 512
 
 
 def a_on_chip(dtype: str, k: int, n: int, chosen: dict) -> int:
-    """After the K split: int8 problems on the two-SM tile with n <= 256 and k
+    """After the K split: int8 problems on the two-SM tile with n <= 512 and k
     a multiple of 16 widen int8 A inside the GEMM instead of staging an f16
     copy (for a narrow C that copy moves more bytes than the multiply)."""
     return int(dtype == "i8" and chosen["bm"] == 256 and k % 16 == 0 and n <= A_ON_CHIP_MAX_N)
