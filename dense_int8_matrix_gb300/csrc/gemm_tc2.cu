@@ -75,7 +75,6 @@ static_assert(kT2WSmem <= 232448, "widened-A shared memory");
 template <bool WIDEN_A>
 struct T2Ring {
     static constexpr int STAGES = WIDEN_A ? kT2WStages : kT2Stages;
-    static constexpr size_t SMEM = WIDEN_A ? kT2WSmem : kT2Smem;
 };
 
 struct T2Params {
