@@ -29,9 +29,10 @@
 //               MMA costs ~45 cycles of issue whatever N, so two issuers keep
 //               the tensor pipe fed while each waits for its next stage;
 //   warps 12-19 drain each accumulator chunk (two warps per lane quarter,
-//               half of the NP columns each), convert it to int32 (exact),
-//               add it into C (pre-zeroed) with coalesced integer atomics
-//               (exact and order-free) and zero the accumulator again.
+//               half of the NP columns each) into registers, zero and
+//               release the accumulator, then convert the chunk to int32
+//               (exact) and add it into C (pre-zeroed) with coalesced
+//               integer atomics (exact and order-free).
 // Work split ("stream-K"): the (128-row tile, stage) iterations are numbered
 // tile-major and every CTA takes an equal contiguous range, so all SMs
 // stream the same number of Bt bytes.
@@ -423,25 +424,30 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (!got) break;
             tc_fence_after();
             const uint32_t taddr = tmem_acc + buf * NP + col0 + lanes;
-            const int64_t j = static_cast<int64_t>(c.tile) * 128 + jrow;
-            int32_t* out = p.C + static_cast<int64_t>(col0) * p.n + j;
+            // the whole chunk into registers (one wait), the accumulator
+            // zeroed and released at once, and only then the atomics into C,
+            // so the MMAs into this accumulator never wait for them
+            uint32_t v[Cfg::EPI_COLS / 8][8];
 #pragma unroll
-            for (int c0 = 0; c0 < Cfg::EPI_COLS; c0 += 8) {
-                uint32_t v[8];
-                tmem_ld_32x32b_x8(taddr + c0, v);
-                tmem_wait_ld();
-                tmem_st_32x32b_x8(taddr + c0, zero);
-                if (j < p.n) {
+            for (int g8 = 0; g8 < Cfg::EPI_COLS / 8; ++g8) tmem_ld_32x32b_x8(taddr + g8 * 8, v[g8]);
+            tmem_wait_ld();
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        if (c0 + cc < rows)
-                            atomicAdd(out + static_cast<int64_t>(c0 + cc) * p.n, __float2int_rn(__uint_as_float(v[cc])));
-                }
-            }
+            for (int g8 = 0; g8 < Cfg::EPI_COLS / 8; ++g8) tmem_st_32x32b_x8(taddr + g8 * 8, zero);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8u * buf);
+            const int64_t j = static_cast<int64_t>(c.tile) * 128 + jrow;
+            if (j < p.n) {
+                int32_t* out = p.C + static_cast<int64_t>(col0) * p.n + j;
+#pragma unroll
+                for (int g8 = 0; g8 < Cfg::EPI_COLS / 8; ++g8)
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc)
+                        if (g8 * 8 + cc < rows)
+                            atomicAdd(out + static_cast<int64_t>(g8 * 8 + cc) * p.n,
+                                      __float2int_rn(__uint_as_float(v[g8][cc])));   // exact
+            }
             ++ch;
         }
     }
