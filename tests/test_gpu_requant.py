@@ -179,3 +179,15 @@ def test_requant_rejects_bad_arguments():
     assert st == B.GEMM_ERR_MISALIGNED
     st = lib.gemm_i8_run_requant(ctypes.byref(plan), p, p, None, p, B.GEMM_OUT_I8, p, None)
     assert st == B.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("m,k,n", [(4097, 16384, 255), (1000, 4096, 512), (10240, 1024, 256)])
+def test_requant_with_a_widened_on_chip(m, k, n):
+    # plans that widen int8 A inside the two-SM kernel (a_on_chip = 1), with
+    # every tile split along K (the scratch path) or, for (10240, 1024, 256),
+    # whole tiles (40 tiles in one wave: requantised in the epilogue)
+    A, Bt, rs, cs = _case(m, k, n, 110 + n)
+    plan = B.gemm_i8_plan(m, k, n)
+    assert plan.a_on_chip == 1
+    for out in ("bf16", "i8"):
+        assert_requant_exact(A, Bt, rs, cs, out, gpu_requant(A, Bt, rs, cs, out, plan=plan))

@@ -121,6 +121,15 @@ def test_noalloc_k_split_plan(m, k, n):
     assert torch.equal(out, ref)
 
 
+def test_noalloc_plan_that_widens_a_on_chip():
+    # a plan with a_on_chip = 1 runs on the staged path here (the f16 copy of
+    # A in the static array), with the same result
+    plan = B.gemm_i8_plan(2048, 4096, 255)
+    assert plan.a_on_chip == 1
+    out, ref = _both(2048, 4096, 255, 90)
+    assert torch.equal(out, ref)
+
+
 def test_noalloc_takes_nothing_from_the_pool():
     # the library pool's high-water mark stays at zero across tensor-path and
     # skinny calls of the allocation-free entry point, while one gemm_i8_run
