@@ -775,6 +775,19 @@ def test_i8_a_on_chip(m, k, n, split):
     G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt, plan=p))
 
 
+@pytest.mark.parametrize("m,k,n,split,grid", [
+    (2000, 1936, 500, 1, 4),    # 16 whole tiles of 31 K steps (odd) on 2 pairs
+    (700, 3008, 300, 3, 2),     # 6 tiles x 3 K slices of 15-16 steps on one pair
+])
+def test_i8_a_on_chip_many_units_per_pair(m, k, n, split, grid):
+    # each pair runs several units back to back, so the int8 boxes of one
+    # unit follow another's in the same ring, also after an odd step count
+    A = workloads.random_i8((m, k), 204)
+    Bt = workloads.random_i8((n, k), 205)
+    p = a_on_chip_plan(m, k, n, 1, split, grid)
+    G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt, plan=p))
+
+
 def test_i8_a_on_chip_extremes_and_repeat():
     # all -128 (every fp32 chunk reaches exactly 2^24) and alternating signs,
     # twice in a row into a poisoned C
