@@ -264,6 +264,61 @@ __device__ __forceinline__ void store_slice32(const CUtensorMap* tmC, const T2Pa
     }
 }
 
+// Row buffers for adding a split tile's last sums into C whose rows are not
+// 16-byte aligned (no TMA): 128 values per row at a shift of 0-3 slots, in
+// rows of 132 slots (528 bytes: the quarter-warp's eight 16-byte stores land
+// in eight different bank groups), 32 rows per epilogue warp.  They reuse
+// the operand rings (with the int8 ring behind the f16 one when A is widened
+// on chip), which are idle once the CTA pair's last unit has left them.
+constexpr int kT2RowSlots = kT2Half2 + 4;
+constexpr int kT2RowBytes = kT2RowSlots * 4;
+constexpr int kT2RowBufBytes = 32 * kT2RowBytes;
+static_assert(kTcEpilogueWarps * kT2RowBufBytes <= kT2WStages * kT2StageBytes + kT2W8Stages * kT2W8Bytes &&
+                  kTcEpilogueWarps * kT2RowBufBytes <= kT2Stages * kT2StageBytes,
+              "row buffers fit in the operand rings");
+
+// This lane's row of 128 sums into its row buffer, value c at slot c + A.
+template <int A>
+__device__ __forceinline__ void put_row_shifted(uint32_t buf, const int32_t (&acc)[kT2Half2]) {
+#pragma unroll
+    for (int i = 0; i < kT2RowSlots / 4; ++i) {
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = 4 * i + j - A;
+            v[j] = (c >= 0 && c < kT2Half2) ? static_cast<uint32_t>(acc[c]) : 0u;
+        }
+        st_shared_v4(buf + 16 * i, v[0], v[1], v[2], v[3]);
+    }
+}
+
+// Add this lane's row of a split tile (128 columns from col0) into C: the
+// 16-byte-aligned middle with one bulk reduce-add from the row buffer, the
+// (at most three) values before and after it with atomics.  Columns past n
+// and rows past m are not touched.
+__device__ __forceinline__ void add_row_bulk(const T2Params& p, const int32_t (&acc)[kT2Half2], uint32_t buf, int row,
+                                             int col0) {
+    if (row >= p.m || col0 >= p.n) return;
+    const int nv = static_cast<int>(min(static_cast<int64_t>(kT2Half2), p.n - col0));
+    uint32_t* out = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc + col0;
+    const int a = static_cast<int>((reinterpret_cast<uintptr_t>(out) >> 2) & 3u);   // slots before out's 16-byte group
+    switch (a) {
+        case 0: put_row_shifted<0>(buf, acc); break;
+        case 1: put_row_shifted<1>(buf, acc); break;
+        case 2: put_row_shifted<2>(buf, acc); break;
+        default: put_row_shifted<3>(buf, acc); break;
+    }
+    fence_proxy_async_smem();   // the bulk copy (async proxy) reads what this thread wrote
+    const int lo = (a + 3) & ~3, hi = (a + nv) & ~3;   // aligned slots [lo, hi)
+    if (hi > lo) {
+        bulk_reduce_add_u32(out + (lo - a), buf + 4 * lo, static_cast<uint32_t>(4 * (hi - lo)));
+        bulk_commit();
+    }
+    // the ends: slots [a, lo) and [max(hi, lo), a + nv)
+    for (int t = a; t < lo && t < a + nv; ++t) atomicAdd(out + (t - a), ld_shared_u32(buf + 4 * t));
+    for (int t = max(hi, lo); t < a + nv; ++t) atomicAdd(out + (t - a), ld_shared_u32(buf + 4 * t));
+}
+
 template <bool INT_OUT, bool C_TMA, bool WIDEN_A>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -583,6 +638,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         continue;
                     }
+                    if (!C_TMA && w.split_tile >= 0 && u + npairs >= p.units) {
+                        // the pair's last unit: its operand ring is idle (all
+                        // MMAs done), so the rows go out by bulk reduce-add
+                        add_row_bulk(p, acc, sA + e * kT2RowBufBytes + lane * kT2RowBytes, row, col0);
+                        continue;
+                    }
 #pragma unroll
                     for (int sl = 0; sl < kT2Half2 / 32; ++sl) {
                         uint32_t r[32];
@@ -611,6 +672,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if constexpr (C_TMA) {
         if (warp >= 4 && lane == 0) bulk_wait_all();
+    } else {
+        if (warp >= 4) bulk_wait_all();   // the rows' bulk reduce-adds (none issued is fine)
     }
     tc_fence_before();
     cluster_sync();   // the peer may still read this CTA's shared memory or barriers until here

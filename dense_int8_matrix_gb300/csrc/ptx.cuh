@@ -135,6 +135,16 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* desc, uint32_t src
                  : "memory");
 }
 
+// Bulk (non-tensor) reduce-add of `bytes` u32 values from shared memory into
+// global memory (bulk-group completion): both addresses 16-byte aligned,
+// `bytes` a multiple of 16.  Integer addition is exact and order-free.
+__device__ __forceinline__ void bulk_reduce_add_u32(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
 // Order generic-proxy global accesses with async-proxy (TMA) ones.
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");

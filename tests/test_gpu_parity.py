@@ -788,6 +788,26 @@ def test_i8_a_on_chip_many_units_per_pair(m, k, n, split, grid):
     G.assert_i8_exact(A, Bt, G.gpu_i8(A, Bt, plan=p))
 
 
+@pytest.mark.parametrize("on", [0, 1])
+@pytest.mark.parametrize("n,offset", [(255, 1), (256, 1), (257, 3), (255, 2), (384, 3)])
+def test_i8_pair_split_unaligned_c(n, offset, on):
+    # K-split tiles on the two-SM kernel adding into a C whose rows are not
+    # 16-byte aligned (n % 4 != 0, or C starting 4-12 bytes into its
+    # allocation): each row's aligned middle goes out by bulk reduce-add, its
+    # ends by atomics; every element exact, nothing outside C touched
+    m, k = 513, 2048
+    A = workloads.random_i8((m, k), 206 + n)
+    Bt = workloads.random_i8((n, k), 207 + offset)
+    p = a_on_chip_plan(m, k, n, on, 3)
+    base = torch.full((m * n + 8,), -7, dtype=torch.int32, device="cuda")
+    C = base[offset:offset + m * n].view(m, n)
+    B.gemm_i8_run(p, A.cuda(), Bt.cuda(), C)
+    torch.cuda.synchronize()
+    G.assert_i8_exact(A, Bt, C.cpu())
+    assert torch.all(base[:offset] == -7) and torch.all(base[offset + m * n:] == -7)
+    assert B.gemm_device_error() == (B.GEMM_OK, 0)
+
+
 def test_i8_a_on_chip_extremes_and_repeat():
     # all -128 (every fp32 chunk reaches exactly 2^24) and alternating signs,
     # twice in a row into a poisoned C
