@@ -319,6 +319,61 @@ __device__ __forceinline__ void add_row_bulk(const T2Params& p, const int32_t (&
     for (int t = max(hi, lo); t < a + nv; ++t) atomicAdd(out + (t - a), ld_shared_u32(buf + 4 * t));
 }
 
+// Whole rows of C per tile (n <= 256, C's row pitch n): the 128 rows of a
+// CTA's half tile are one contiguous run of C.  Each epilogue thread puts its
+// row's sums into an image of that run in the idle operand ring (value j of
+// the run at slot j + a, a = the run's start modulo 16 bytes, in elements),
+// and once all eight epilogue warps have done so one thread moves the
+// 16-byte-aligned middle with a few bulk copies, or bulk reduce-adds for a
+// split tile, and the at most three values at each end with plain stores or
+// atomics.  Rows past m are not in the run.
+constexpr int kT2FlatPieces = 8;   // bulk operations per run
+static_assert(kT2Half * kT2Cols * 4 + 16 <= kT2WStages * kT2StageBytes + kT2W8Stages * kT2W8Bytes &&
+                  kT2Half * kT2Cols * 4 + 16 <= kT2Stages * kT2StageBytes,
+              "run image fits in the operand rings");
+
+__device__ __forceinline__ int flat_shift(const T2Params& p, int row0) {
+    const uint32_t* run = static_cast<const uint32_t*>(p.C) + static_cast<int64_t>(row0) * p.n;
+    return static_cast<int>((reinterpret_cast<uintptr_t>(run) >> 2) & 3u);
+}
+
+__device__ __forceinline__ void put_flat(const T2Params& p, const int32_t (&acc)[kT2Half2], uint32_t img, int a,
+                                         int row0, int row, int col0) {
+    if (row >= p.m) return;
+    const int nv = static_cast<int>(p.n) - col0;   // valid columns of this thread's 128
+    const uint32_t base = img + 4u * static_cast<uint32_t>(a + (row - row0) * static_cast<int>(p.n) + col0);
+#pragma unroll
+    for (int c = 0; c < kT2Half2; ++c)
+        if (c < nv) st_shared_u32(base + 4u * c, static_cast<uint32_t>(acc[c]));
+}
+
+__device__ __forceinline__ void move_flat(const T2Params& p, uint32_t img, int a, int row0, bool add) {
+    const int rows = static_cast<int>(min(static_cast<int64_t>(kT2Half), p.m - row0));
+    if (rows <= 0) return;
+    const int count = rows * static_cast<int>(p.n);   // values in the run
+    uint32_t* run = static_cast<uint32_t*>(p.C) + static_cast<int64_t>(row0) * p.n;
+    const int lo = (a + 3) & ~3, hi = (a + count) & ~3;   // aligned slots [lo, hi)
+    if (hi > lo) {
+        const int per = 4 * ((hi - lo + 4 * kT2FlatPieces - 1) / (4 * kT2FlatPieces));   // >= 4 slots
+        for (int s0 = lo; s0 < hi; s0 += per) {
+            const int s1 = min(hi, s0 + per);
+            if (add)
+                bulk_reduce_add_u32(run + (s0 - a), img + 4u * s0, static_cast<uint32_t>(4 * (s1 - s0)));
+            else
+                bulk_store(run + (s0 - a), img + 4u * s0, static_cast<uint32_t>(4 * (s1 - s0)));
+        }
+        bulk_commit();
+    }
+    for (int t = a; t < a + count && t < lo; ++t) {
+        const uint32_t v = ld_shared_u32(img + 4u * t);
+        if (add) atomicAdd(run + (t - a), v); else run[t - a] = v;
+    }
+    for (int t = max(hi, lo); t < a + count; ++t) {
+        const uint32_t v = ld_shared_u32(img + 4u * t);
+        if (add) atomicAdd(run + (t - a), v); else run[t - a] = v;
+    }
+}
+
 template <bool INT_OUT, bool C_TMA, bool WIDEN_A>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -341,7 +396,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t done_bar = acce_bar0 + 16u;
     const uint32_t a8full_bar0 = done_bar + 8u;             // [kT2W8Stages] int8 A landed (local)
     const uint32_t a8empty_bar0 = a8full_bar0 + 8u * kT2W8Stages;   // [kT2W8Stages] int8 A read (local)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kStages + 5 + 2 * kT2W8Stages));
+    const uint32_t flat_bar = a8empty_bar0 + 8u * kT2W8Stages;      // the epilogue warps' run image is complete
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kStages + 5 + 2 * kT2W8Stages + 1));
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -365,6 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(acce_bar0 + 8u * b, 2 * kTcEpilogueWarps);
         }
         mbar_init(done_bar, 1);
+        mbar_init(flat_bar, kTcEpilogueWarps);
         if constexpr (WIDEN_A) {
             for (int s = 0; s < kT2W8Stages; ++s) {
                 mbar_init(a8full_bar0 + 8u * s, 1);
@@ -635,6 +692,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                             for (int j = 0; j < 8; ++j) t[j] = acc[g * 8 + j];
                             requant_store8(p.rq, p.m, p.n, row, col0 + g * 8, rs, t);
+                        }
+                        continue;
+                    }
+                    if (!C_TMA && p.tiles_n == 1 && p.ldc == p.n && u + npairs >= p.units) {
+                        // the pair's last unit, and its tile holds whole rows
+                        // of C: the operand ring is idle (all MMAs done), so
+                        // this CTA's 128 rows go out as one run
+                        const int a = flat_shift(p, row0);
+                        put_flat(p, acc, sA, a, row0, row, col0);
+                        fence_proxy_async_smem();   // the bulk copies (async proxy) read the image
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(flat_bar);
+                        if (warp == 4 && lane == 0) {
+                            if (wait_bounded(flat_bar, 0u, abort_flag, p.err, kDevErrTimeoutEpilogue))
+                                move_flat(p, sA, a, row0, w.split_tile >= 0);
                         }
                         continue;
                     }

@@ -145,6 +145,18 @@ __device__ __forceinline__ void bulk_reduce_add_u32(void* dst, uint32_t src, uin
                  : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` from shared to global memory (bulk-group
+// completion): both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t a) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
+}
+
 // Order generic-proxy global accesses with async-proxy (TMA) ones.
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
