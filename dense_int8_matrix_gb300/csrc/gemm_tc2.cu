@@ -695,10 +695,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         continue;
                     }
-                    if (!C_TMA && p.tiles_n == 1 && p.ldc == p.n && u + npairs >= p.units) {
+                    if (!C_TMA && p.tiles_n == 1 && (p.n & 1) && p.ldc == p.n && u + npairs >= p.units) {
                         // the pair's last unit, and its tile holds whole rows
                         // of C: the operand ring is idle (all MMAs done), so
-                        // this CTA's 128 rows go out as one run
+                        // this CTA's 128 rows go out as one run (odd n only:
+                        // the lanes' rows then start in different banks of
+                        // the image; even n would make its stores conflict)
                         const int a = flat_shift(p, row0);
                         put_flat(p, acc, sA, a, row0, row, col0);
                         fence_proxy_async_smem();   // the bulk copies (async proxy) read the image

@@ -139,17 +139,17 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* desc, uint32_t src
 // global memory (bulk-group completion): both addresses 16-byte aligned,
 // `bytes` a multiple of 16.  Integer addition is exact and order-free.
 __device__ __forceinline__ void bulk_reduce_add_u32(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(
-                     reinterpret_cast<uint64_t>(dst)),
-                 "r"(src), "r"(bytes)
+    const uint64_t g = static_cast<uint64_t>(__cvta_generic_to_global(dst));   // .global address
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(g), "r"(src),
+                 "r"(bytes)
                  : "memory");
 }
 
 // Bulk (non-tensor) copy of `bytes` from shared to global memory (bulk-group
 // completion): both addresses 16-byte aligned, `bytes` a multiple of 16.
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
-                 "r"(src), "r"(bytes)
+    const uint64_t g = static_cast<uint64_t>(__cvta_generic_to_global(dst));   // .global address
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g), "r"(src), "r"(bytes)
                  : "memory");
 }
 

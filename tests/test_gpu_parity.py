@@ -790,14 +790,14 @@ def test_i8_a_on_chip_many_units_per_pair(m, k, n, split, grid):
 
 @pytest.mark.parametrize("on", [0, 1])
 @pytest.mark.parametrize("n,offset,split", [(255, 1, 3), (256, 1, 3), (257, 3, 3), (255, 2, 3), (384, 3, 3),
-                                            (255, 0, 1), (200, 1, 1), (129, 2, 1), (300, 3, 1)])
+                                            (255, 0, 1), (200, 1, 1), (129, 2, 1), (300, 3, 1), (1, 0, 3)])
 def test_i8_pair_unaligned_c(n, offset, split, on):
     # the two-SM kernel writing (whole tiles) or adding (K-split tiles) into a
     # C whose rows are not 16-byte aligned (n % 4 != 0, or C starting 4-12
-    # bytes into its allocation): with n <= 256 a CTA's rows go out as one
-    # contiguous run by bulk copies or reduce-adds, wider C row by row; the
-    # unaligned ends by plain stores or atomics; every element exact,
-    # nothing outside C touched
+    # bytes into its allocation): with odd n <= 256 a CTA's rows go out as
+    # one contiguous run by bulk copies or reduce-adds, other split tiles row
+    # by row; the unaligned ends by plain stores or atomics; every element
+    # exact, nothing outside C touched
     m, k = 513, 2048
     A = workloads.random_i8((m, k), 206 + n)
     Bt = workloads.random_i8((n, k), 207 + offset)
