@@ -29,14 +29,19 @@
 // int8 A is loaded by TMA (128 rows x 128 bytes, two K steps, per box) into a
 // separate ring, and warps 2 and 3 of each CTA (one K step of each box) widen
 // it exactly to f16 in the 128-byte swizzled layout of the operand ring, so A
-// crosses HBM once, as int8; Bt still comes from the staged f16 copy.  The widened halves of both CTAs are
-// announced on the even CTA's "full" barrier beside the TMA bytes of Bt.
+// crosses HBM once, as int8; Bt still comes from the staged f16 copy.  The
+// widened halves of both CTAs are announced on the even CTA's "full" barrier
+// beside the TMA bytes of Bt.
 //
 // Tail split (int8 problems): when the last round of pairs is only partly
 // filled, the tiles of that round run as split_k K slices on otherwise idle
 // pairs.  The staging kernel zeroes C over those tiles, and every slice adds
-// its exact int32 partial sums into C with a TMA reduce-add (atomics when C
-// cannot take TMA): no slice waits on another, whatever order the pairs run in.
+// its exact int32 partial sums into C with a TMA reduce-add: no slice waits
+// on another, whatever order the pairs run in.  When C's rows are not 16-byte
+// aligned (no TMA), a pair's last unit uses its idle operand ring as staging
+// for bulk copies or reduce-adds (a contiguous run of whole rows for odd
+// n <= 256, row by row otherwise); earlier units go through the transposed
+// 32 x 32 staging buffer into warp-wide atomics or stores.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
