@@ -479,15 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                              kDevErrTimeoutTeardown);
         } else if (lane == 0) {
             pdl_wait();   // the operands may come from the staging kernel just before
-            // A's panel is read by every tile of its band of M-tiles (the
-            // tile order walks a band's N tiles before the next band), so it
-            // is kept in L2 in preference to Bt's panels, which only the
-            // band's few concurrent M-tiles share (measured on GB300 at
-            // 8192^3: 1.3 % faster for int8, 2.2 % for bf16; 4096^3 alike).
-            // With A widened on chip, every pair of a K slice reads the same
-            // Bt panel, which stays at the normal priority.
-            const uint64_t pol = WIDEN_A ? policy_evict_normal() : policy_evict_first();
-            const uint64_t pol_a = policy_evict_last();
+            const uint64_t pol = policy_evict_normal();
             uint32_t issued = 0;
             bool ok = true;
             for (int u = pair; ok && u < p.units; u += npairs) {
@@ -511,7 +503,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // both CTAs' copies complete on the even CTA's barrier,
                         // which expects the bytes of both
                         if (leader) mbar_arrive_expect_tx(full_bar0 + 8u * s, 2 * kT2StageBytes);
-                        tma_load_2d_pair(sA + s * kT2HalfBytes, &tmA, kb * kTcBK, ya, fb, pol_a);
+                        tma_load_2d_pair(sA + s * kT2HalfBytes, &tmA, kb * kTcBK, ya, fb, pol);
                     }
                     tma_load_2d_pair(sB + s * kT2HalfBytes, &tmB, kb * kTcBK, yb, fb, pol);
                     ++issued;
