@@ -122,3 +122,16 @@ def test_clock_summary_reasons_and_median():
     assert out["reasons"] == ["sw_power_cap"] and out["samples"] == 3
     empty = bench.ClockSampler(0).summary()
     assert empty["samples"] == 0 and empty["sm_mhz"] is None
+
+
+def test_traffic_records_match_the_kernel_sources():
+    # the headline's DRAM traffic and the skinny one are reported only while
+    # the kernel sources still match the digest recorded with the ncu capture:
+    # a kernel change must come with a new capture
+    rec = bench.load_traffic()
+    assert rec["i8_8192"][1] == bench.kernel_source_digest("tc")
+    assert rec["i8_skinny_m64"][1] == bench.kernel_source_digest("skinny")
+    # DRAM bytes of one launch: at least the algorithmic bytes each kernel moves
+    k = n = 8192
+    assert rec["i8_8192"][0] >= 2 * 8192 * 8192 * 2 + 4 * 8192 * 8192   # f16 A and Bt once, int32 C
+    assert rec["i8_skinny_m64"][0] >= n * k                           # Bt once
