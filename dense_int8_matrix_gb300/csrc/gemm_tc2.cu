@@ -80,10 +80,23 @@ constexpr size_t kT2WSmem = static_cast<size_t>(kT2WStages) * kT2StageBytes +
                             static_cast<size_t>(kT2W8Stages) * kT2W8Bytes + kT2EpiBytes + 1024 + 1024;
 static_assert(kT2WSmem <= 232448, "widened-A shared memory");
 
-template <bool WIDEN_A>
+// Shared-memory rings of one kernel instance.  DEEP (widened A only): an
+// instance for launches whose epilogue never stages C, i.e. whose every unit
+// is its pair's last and goes out as a contiguous run (odd n <= 256, C's
+// pitch n, no more units than pairs; the launch checks this): the 32 KiB of C
+// staging go to a fifth f16 stage (measured on GB300: (4097, 16384, 255)
+// 39.1 -> 37.5 us, (16384, 16384, 255) 102.2 -> 97.1 us).
+template <bool WIDEN_A, bool DEEP = false>
 struct T2Ring {
-    static constexpr int STAGES = WIDEN_A ? kT2WStages : kT2Stages;
+    static_assert(!DEEP || WIDEN_A, "the deep rings are a widened-A layout");
+    static constexpr int STAGES = DEEP ? 5 : (WIDEN_A ? kT2WStages : kT2Stages);
+    static constexpr int W8 = DEEP ? 3 : kT2W8Stages;   // int8 boxes
+    static constexpr int EPI = DEEP ? 0 : kT2EpiBytes;  // C staging bytes
+    static constexpr size_t SMEM = static_cast<size_t>(STAGES) * kT2StageBytes +
+                                   (WIDEN_A ? static_cast<size_t>(W8) * kT2W8Bytes : 0) + EPI + 1024 + 1024;
 };
+static_assert(T2Ring<false>::SMEM == kT2Smem && T2Ring<true>::SMEM == kT2WSmem, "ring layouts");
+static_assert(T2Ring<true, true>::SMEM <= 232448, "deep widened-A shared memory");
 
 struct T2Params {
     void* C;
@@ -334,7 +347,9 @@ __device__ __forceinline__ void add_row_bulk(const T2Params& p, const int32_t (&
 // atomics.  Rows past m are not in the run.
 constexpr int kT2FlatPieces = 8;   // bulk operations per run
 static_assert(kT2Half * kT2Cols * 4 + 16 <= kT2WStages * kT2StageBytes + kT2W8Stages * kT2W8Bytes &&
-                  kT2Half * kT2Cols * 4 + 16 <= kT2Stages * kT2StageBytes,
+                  kT2Half * kT2Cols * 4 + 16 <= kT2Stages * kT2StageBytes &&
+                  kT2Half * kT2Cols * 4 + 16 <=
+                      T2Ring<true, true>::STAGES * kT2StageBytes + T2Ring<true, true>::W8 * kT2W8Bytes,
               "run image fits in the operand rings");
 
 __device__ __forceinline__ int flat_shift(const T2Params& p, int row0) {
@@ -379,30 +394,33 @@ __device__ __forceinline__ void move_flat(const T2Params& p, uint32_t img, int a
     }
 }
 
-template <bool INT_OUT, bool C_TMA, bool WIDEN_A>
+template <bool INT_OUT, bool C_TMA, bool WIDEN_A, bool DEEP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const T2Params p) {
     static_assert(!WIDEN_A || INT_OUT, "A is widened from int8 only");
-    constexpr int kStages = T2Ring<WIDEN_A>::STAGES;
+    static_assert(!DEEP || !C_TMA, "the deep rings have no C staging");
+    using Ring = T2Ring<WIDEN_A, DEEP>;
+    constexpr int kStages = Ring::STAGES;
+    constexpr int kW8 = Ring::W8;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sA = base;
     const uint32_t sB = base + kStages * kT2HalfBytes;
     const uint32_t sA8 = base + kStages * kT2StageBytes;   // int8 A ring (widened-A variant)
-    const uint32_t sEpi = sA8 + (WIDEN_A ? kT2W8Stages * kT2W8Bytes : 0);
-    uint8_t* ctrl = smem_raw + (sEpi - raw) + kT2EpiBytes;
+    const uint32_t sEpi = sA8 + (WIDEN_A ? kW8 * kT2W8Bytes : 0);   // (DEEP: no C staging)
+    uint8_t* ctrl = smem_raw + (sEpi - raw) + Ring::EPI;
     const uint32_t bar0 = smem_u32(ctrl);
     const uint32_t full_bar0 = bar0;                        // used in the even CTA
     const uint32_t empty_bar0 = bar0 + 8u * kStages;
     const uint32_t accf_bar0 = bar0 + 16u * kStages;
     const uint32_t acce_bar0 = accf_bar0 + 16u;             // used in the even CTA
     const uint32_t done_bar = acce_bar0 + 16u;
-    const uint32_t a8full_bar0 = done_bar + 8u;             // [kT2W8Stages] int8 A landed (local)
-    const uint32_t a8empty_bar0 = a8full_bar0 + 8u * kT2W8Stages;   // [kT2W8Stages] int8 A read (local)
-    const uint32_t flat_bar = a8empty_bar0 + 8u * kT2W8Stages;      // the epilogue warps' run image is complete
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kStages + 5 + 2 * kT2W8Stages + 1));
+    const uint32_t a8full_bar0 = done_bar + 8u;             // [kW8] int8 A landed (local)
+    const uint32_t a8empty_bar0 = a8full_bar0 + 8u * kW8;   // [kW8] int8 A read (local)
+    const uint32_t flat_bar = a8empty_bar0 + 8u * kW8;      // the epilogue warps' run image is complete
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kStages + 5 + 2 * kW8 + 1));
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -428,7 +446,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(done_bar, 1);
         mbar_init(flat_bar, kTcEpilogueWarps);
         if constexpr (WIDEN_A) {
-            for (int s = 0; s < kT2W8Stages; ++s) {
+            for (int s = 0; s < kW8; ++s) {
                 mbar_init(a8full_bar0 + 8u * s, 1);
                 mbar_init(a8empty_bar0 + 8u * s, kT2W8Steps);   // both widening warps
             }
@@ -450,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (WIDEN_A && lane == 1) {
             // int8 A into its own ring, gated only by the widening warps'
             // releases (not by the f16 slots), so the HBM stream runs up to
-            // kT2W8Stages boxes ahead.  A unit's box j holds its K steps
+            // kW8 boxes ahead.  A unit's box j holds its K steps
             // kb_lo + 2j and kb_lo + 2j + 1 (the second unused past kb_hi)
             pdl_wait();
             const uint64_t pol = policy_evict_first();
@@ -460,7 +478,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const Unit2 w = unit_at2(u, p);
                 const int ya = w.tm * 256 + static_cast<int>(rank) * kT2Half;
                 for (int kb = w.kb_lo; kb < w.kb_hi; kb += kT2W8Steps) {
-                    const uint32_t s8 = issued % kT2W8Stages, ph8 = (issued / kT2W8Stages) & 1u;
+                    const uint32_t s8 = issued % kW8, ph8 = (issued / kW8) & 1u;
                     if (!wait_bounded(a8empty_bar0 + 8u * s8, ph8 ^ 1u, abort_flag, p.err, kDevErrTimeoutProducer)) {
                         ok = false;
                         break;
@@ -473,9 +491,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Teardown: the copies still in flight must land before the CTA
             // exits (earlier ones were waited for by the widening group
             // before their slot was reused)
-            for (uint32_t j = issued > static_cast<uint32_t>(kT2W8Stages) ? issued - kT2W8Stages : 0u; j < issued;
-                 ++j)
-                wait_bounded(a8full_bar0 + 8u * (j % kT2W8Stages), (j / kT2W8Stages) & 1u, nullptr, p.err,
+            for (uint32_t j = issued > static_cast<uint32_t>(kW8) ? issued - kW8 : 0u; j < issued; ++j)
+                wait_bounded(a8full_bar0 + 8u * (j % kW8), (j / kW8) & 1u, nullptr, p.err,
                              kDevErrTimeoutTeardown);
         } else if (lane == 0) {
             pdl_wait();   // the operands may come from the staging kernel just before
@@ -535,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t d = done + static_cast<uint32_t>(rel);   // this K step, counted over units
                 const uint32_t bx = box + static_cast<uint32_t>(rel / kT2W8Steps);
                 const uint32_t s = d % kStages, ph = (d / kStages) & 1u;
-                const uint32_t s8 = bx % kT2W8Stages, ph8 = (bx / kT2W8Stages) & 1u;
+                const uint32_t s8 = bx % kW8, ph8 = (bx / kW8) & 1u;
                 int got = 1;
                 if (lane == 0)
                     got = (wait_bounded(a8full_bar0 + 8u * s8, ph8, abort_flag, p.err, kDevErrTimeoutProducer) &&
@@ -577,7 +594,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (ok && (steps % kT2W8Steps) != 0 && h == 1) {
                 // the unit's last box has no second step: release it unread
                 const uint32_t bx = box + static_cast<uint32_t>(steps / kT2W8Steps);
-                const uint32_t s8 = bx % kT2W8Stages, ph8 = (bx / kT2W8Stages) & 1u;
+                const uint32_t s8 = bx % kW8, ph8 = (bx / kW8) & 1u;
                 if (lane == 0) {
                     if (wait_bounded(a8full_bar0 + 8u * s8, ph8, abort_flag, p.err, kDevErrTimeoutProducer))
                         mbar_arrive(a8empty_bar0 + 8u * s8);
@@ -700,6 +717,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         continue;
                     }
+                    if constexpr (DEEP) {
+                        if (!(p.tiles_n == 1 && (p.n & 1) && p.ldc == p.n && u + npairs >= p.units)) {
+                            // not reached (the launch picks these rings only
+                            // when every unit leaves as a run): with no C
+                            // staging there is no other way out, so the call
+                            // ends with an error and C incomplete
+                            if (lane == 0) {
+                                atomicCAS(p.err, 0, kDevErrTimeoutEpilogue);
+                                *abort_flag = 1u;
+                            }
+                            continue;
+                        }
+                    }
                     if (!C_TMA && p.tiles_n == 1 && (p.n & 1) && p.ldc == p.n && u + npairs >= p.units) {
                         // the pair's last unit, and its tile holds whole rows
                         // of C: the operand ring is idle (all MMAs done), so
@@ -776,9 +806,9 @@ bool encode(CUtensorMap* map, CUtensorMapDataType type, void* ptr, uint64_t inne
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool INT_OUT, bool C_TMA, bool WIDEN_A = false>
+template <bool INT_OUT, bool C_TMA, bool WIDEN_A = false, bool DEEP = false>
 const void* tc2_kernel_ptr() {
-    return reinterpret_cast<const void*>(gemm_tc2_kernel<INT_OUT, C_TMA, WIDEN_A>);
+    return reinterpret_cast<const void*>(gemm_tc2_kernel<INT_OUT, C_TMA, WIDEN_A, DEEP>);
 }
 
 cudaError_t configure2(const void* kern, size_t smem = kT2Smem) {
@@ -872,10 +902,14 @@ cudaError_t launch_tc2(const TcLaunch& a, int max_pairs, cudaStream_t stream) {
     p.units = p.split_from + (p.tiles - p.split_from) * p.split_k;
     p.rq = requant ? a.rq : RqOut{};
     const int pairs = tc2_pairs_for(a.grid, max_pairs, p.units);
-    const void* kern = widen ? (c_tma ? tc2_kernel_ptr<true, true, true>() : tc2_kernel_ptr<true, false, true>())
+    // the deep widened-A rings: every unit is its pair's last (units <= pairs)
+    // and leaves as a contiguous run of whole rows (odd n <= 256, pitch n)
+    const bool deep = widen && !c_tma && p.tiles_n == 1 && (a.n & 1) && ldc == a.n && p.units <= pairs;
+    const void* kern = deep ? tc2_kernel_ptr<true, false, true, true>()
+                       : widen ? (c_tma ? tc2_kernel_ptr<true, true, true>() : tc2_kernel_ptr<true, false, true>())
                        : a.int_out ? (c_tma ? tc2_kernel_ptr<true, true>() : tc2_kernel_ptr<true, false>())
                                    : (c_tma ? tc2_kernel_ptr<false, true>() : tc2_kernel_ptr<false, false>());
-    const size_t smem = widen ? kT2WSmem : kT2Smem;
+    const size_t smem = deep ? T2Ring<true, true>::SMEM : widen ? kT2WSmem : kT2Smem;
     cudaError_t e = configure2(kern, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;

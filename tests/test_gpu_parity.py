@@ -778,6 +778,8 @@ def test_i8_a_on_chip(m, k, n, split):
 @pytest.mark.parametrize("m,k,n,split,grid", [
     (2000, 1936, 500, 1, 4),    # 16 whole tiles of 31 K steps (odd) on 2 pairs
     (700, 3008, 300, 3, 2),     # 6 tiles x 3 K slices of 15-16 steps on one pair
+    (2000, 1936, 255, 1, 4),    # odd n <= 256 but more units than pairs: the
+    (700, 3008, 255, 3, 2),     # rings with C staging, runs only for the last unit
 ])
 def test_i8_a_on_chip_many_units_per_pair(m, k, n, split, grid):
     # each pair runs several units back to back, so the int8 boxes of one
